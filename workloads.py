@@ -1,0 +1,242 @@
+"""Seeded synthetic inputs for per-query top-k selection with paged slot translation.
+
+This module only draws random numbers and lays them out as arrays (score rows,
+valid lengths, block tables). It holds none of the selection or slot arithmetic,
+so both the CPU oracle and the CUDA path can consume its batches without sharing
+any of the method's code.
+
+Workloads follow the indexer top-k setting of "Serving GLM5.2 NVFP4 Agentic
+Workload with SGLang" (section "Kernel Optimization > TopK-V2", Fig. 4): fp32
+score rows over the historical KV positions of each query, k up to 2048, KV pages
+of 64 tokens ("llm-d ... GLM-5.2 on H200", KV block size). The agentic replay
+corpus measured there is not available; the distributions below stand in for it.
+
+Every batch stores scores as float32 [rows, ld] with ld >= max_len. Entries at
+positions >= lens[r] are poisoned with +3e38 so that any out-of-range read would
+win the selection and fail parity loudly.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional
+
+import numpy as np
+
+POISON = np.float32(3.0e38)
+SEED_BASE = 0x5EED0000
+
+
+@dataclasses.dataclass
+class Batch:
+    """One call's worth of inputs (k may be varied by the caller per call)."""
+
+    name: str
+    scores: np.ndarray            # float32 [rows, ld]
+    lens: np.ndarray              # int32 [rows]
+    max_len: int
+    k: int
+    block_table: np.ndarray       # int32 [n_tables, table_ld]
+    row_to_table: Optional[np.ndarray]  # int32 [rows] or None (identity)
+    page_size: int
+    ks: Optional[List[int]] = None  # per-call k sequence, where the workload defines one
+
+    @property
+    def rows(self) -> int:
+        return int(self.scores.shape[0])
+
+    @property
+    def ld(self) -> int:
+        return int(self.scores.shape[1])
+
+    def algorithmic_bytes(self, k: Optional[int] = None, with_pos: bool = False) -> int:
+        """Scores read once + each distinct table's used pages once + the slot output."""
+        k = self.k if k is None else k
+        score_b = 4 * int(self.lens.astype(np.int64).sum())
+        r2t = (np.arange(self.rows, dtype=np.int64) if self.row_to_table is None
+               else self.row_to_table.astype(np.int64))
+        pages = 0
+        for t in np.unique(r2t):
+            lmax = int(self.lens[r2t == t].max()) if self.rows else 0
+            pages += -(-lmax // self.page_size)
+        out_b = 4 * self.rows * k * (2 if with_pos else 1)
+        return score_b + 4 * pages + out_b
+
+
+def round_up(x: int, m: int) -> int:
+    return -(-x // m) * m
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _empty_scores(rows: int, ld: int) -> np.ndarray:
+    s = np.empty((rows, ld), dtype=np.float32)
+    s.fill(POISON)
+    return s
+
+
+def _shuffled_pages(rng: np.random.Generator, n: int) -> np.ndarray:
+    return rng.permutation(n).astype(np.int32)
+
+
+def _tables_from_pool(rng, lens, page_size, table_ld):
+    """One table row per request; pages drawn without replacement from one shuffled pool.
+    Unused entries are -1 (a null placeholder that must never be read)."""
+    need = [-(-int(l) // page_size) for l in lens]
+    pool = _shuffled_pages(rng, max(1, sum(need)))
+    tab = np.full((len(lens), table_ld), -1, dtype=np.int32)
+    off = 0
+    for r, n in enumerate(need):
+        tab[r, :n] = pool[off:off + n]
+        off += n
+    return tab
+
+
+def pr1(seed: int = SEED_BASE + 0) -> Batch:
+    """4 rows, lens {4096, 5000, 6144, 8192}, k=2048, N(0,1), page_size 64,
+    block tables = a random permutation of 4*128 page ids sliced 128 per row."""
+    rng = _rng(seed)
+    lens = np.array([4096, 5000, 6144, 8192], dtype=np.int32)
+    max_len = 8192
+    s = _empty_scores(4, round_up(max_len, 4))
+    for r, l in enumerate(lens):
+        s[r, :l] = rng.standard_normal(l).astype(np.float32)
+    perm = _shuffled_pages(rng, 512)
+    tab = perm.reshape(4, 128).copy()
+    return Batch("pr1_ref", s, lens, max_len, 2048, tab, None, 64)
+
+
+def tiny_rows(seed: int = SEED_BASE + 10, n_rows: int = 1000, page_size: int = 64):
+    """1000 tiny rows, len U[1, 64], per-row k U[1, 16], values uniform on {-2..2}
+    (massive ties). Returned as one Batch per k value (k is a per-call argument)."""
+    rng = _rng(seed)
+    lens = rng.integers(1, 65, size=n_rows).astype(np.int32)
+    ks = rng.integers(1, 17, size=n_rows)
+    max_len = 64
+    vals = rng.integers(-2, 3, size=(n_rows, max_len)).astype(np.float32)
+    tabs = _tables_from_pool(rng, lens, page_size, -(-max_len // page_size))
+    out = []
+    for k in range(1, 17):
+        idx = np.nonzero(ks == k)[0]
+        if idx.size == 0:
+            continue
+        s = _empty_scores(idx.size, max_len)
+        for j, r in enumerate(idx):
+            s[j, :lens[r]] = vals[r, :lens[r]]
+        out.append(Batch(f"tiny_k{k}", s, lens[idx].copy(), max_len, k,
+                         tabs[idx].copy(), None, page_size))
+    return out
+
+
+def verify_80k(seed: int = SEED_BASE + 1) -> Batch:
+    """bs=1 MTP target verify at 80K ISL: 7 rows with causal lengths 80000..80006,
+    k=2048, N(0,1) with 1% of positions given a +3 sigma outlier, page_size 64,
+    one shuffled table of 1251 pages shared by the 7 rows."""
+    rng = _rng(seed)
+    lens = np.arange(80000, 80007, dtype=np.int32)
+    max_len = 80006
+    s = _empty_scores(7, round_up(max_len, 4))
+    for r, l in enumerate(lens):
+        x = rng.standard_normal(l)
+        x += 3.0 * (rng.random(l) < 0.01)
+        s[r, :l] = x.astype(np.float32)
+    tab = _shuffled_pages(rng, -(-max_len // 64)).reshape(1, -1)
+    return Batch("verify_80k", s, lens, max_len, 2048, tab,
+                 np.zeros(7, dtype=np.int32), 64)
+
+
+def verify_1m(seed: int = SEED_BASE + 2, amplitude: float = 1.0, period: int = 1 << 18) -> Batch:
+    """bs=1 MTP target verify at 1M ISL: 7 rows with lengths 1,000,000..1,000,006,
+    k=2048, N(0,1) plus a slowly varying sinusoidal bias A*sin(2*pi*p/P) along
+    position (A=1, P=2^18 positions), page_size 64, one shuffled table."""
+    rng = _rng(seed)
+    lens = np.arange(1_000_000, 1_000_007, dtype=np.int32)
+    max_len = 1_000_006
+    s = _empty_scores(7, round_up(max_len, 4))
+    bias = amplitude * np.sin(2.0 * math.pi * np.arange(max_len) / period)
+    for r, l in enumerate(lens):
+        s[r, :l] = (rng.standard_normal(l) + bias[:l]).astype(np.float32)
+    tab = _shuffled_pages(rng, -(-max_len // 64)).reshape(1, -1)
+    return Batch("verify_1m", s, lens, max_len, 2048, tab,
+                 np.zeros(7, dtype=np.int32), 64)
+
+
+def mixed_decode(seed: int = SEED_BASE + 3) -> Batch:
+    """Mixed decode batch: 64 requests x 1 row, lengths log-uniform in [1024, 200000],
+    k=2048, N(0,1), page_size 64, a random page table per request."""
+    rng = _rng(seed)
+    lens = np.floor(np.exp(rng.uniform(math.log(1024), math.log(200000), size=64))).astype(np.int32)
+    lens = np.clip(lens, 1024, 200000)
+    max_len = 200000
+    s = _empty_scores(64, round_up(max_len, 4))
+    for r, l in enumerate(lens):
+        s[r, :l] = rng.standard_normal(l).astype(np.float32)
+    tab = _tables_from_pool(rng, lens, 64, -(-max_len // 64))
+    return Batch("mixed_decode", s, lens, max_len, 2048, tab, None, 64)
+
+
+ADV_KS = (1, 64, 512, 2048)
+
+
+def adversarial(seed: int = SEED_BASE + 4, rows: int = 256, max_len: int = 32768) -> Batch:
+    """256 rows x max_len 32768, page_size 32, 1024-page table per row from one
+    shuffled pool; k drawn per call from {1, 64, 512, 2048}. Row kind = row mod 6:
+    0 all-equal (cycling +/-0 alternating by position, all -0.0, all 1.5);
+    1 N(0,1) rounded to the fp16 grid; 2 N(0,1) prefix then -inf up to len;
+    3 len U[0, 2047] (below the largest k, some exactly 0); 4 Cauchy tan(pi(U-1/2));
+    5 N(0,1) at full length. Lengths of kinds other than 3 and 5 are U[1, max_len]."""
+    rng = _rng(seed)
+    ps = 32
+    lens = np.zeros(rows, dtype=np.int32)
+    s = _empty_scores(rows, round_up(max_len, 4))
+    for r in range(rows):
+        kind, m = r % 6, r // 6
+        if kind == 3:
+            l = 0 if m % 4 == 0 else int(rng.integers(0, 2048))
+        elif kind == 5:
+            l = max_len
+        else:
+            l = int(rng.integers(1, max_len + 1))
+        lens[r] = l
+        if kind == 0:
+            c = m % 3
+            if c == 0:
+                x = np.where(np.arange(l) % 2 == 0, np.float32(0.0), np.float32(-0.0))
+            elif c == 1:
+                x = np.full(l, -0.0, dtype=np.float32)
+            else:
+                x = np.full(l, 1.5, dtype=np.float32)
+        elif kind == 1:
+            x = rng.standard_normal(l).astype(np.float16).astype(np.float32)
+        elif kind == 2:
+            x = rng.standard_normal(l).astype(np.float32)
+            cut = int(rng.integers(0, l + 1))
+            x[cut:] = -np.inf
+        elif kind == 4:
+            x = np.tan(math.pi * (rng.random(l) - 0.5)).astype(np.float32)
+        else:
+            x = rng.standard_normal(l).astype(np.float32)
+        s[r, :l] = x
+    tab = _tables_from_pool(rng, [max_len] * rows, ps, max_len // ps)
+    ks = [int(v) for v in rng.permutation(np.array(ADV_KS))]
+    return Batch("adversarial", s, lens, max_len, ks[0], tab, None, ps, ks=ks)
+
+
+CONFIGS = {
+    "pr1_ref": pr1,
+    "verify_80k": verify_80k,
+    "verify_1m": verify_1m,
+    "mixed_decode": mixed_decode,
+    "adversarial": adversarial,
+}
+
+
+def with_ld(b: Batch, ld: int) -> Batch:
+    """Same rows re-laid with another row stride (e.g. ld = max_len, not a multiple of 4)."""
+    assert ld >= b.max_len
+    s = _empty_scores(b.rows, ld)
+    w = min(ld, b.ld)
+    s[:, :w] = b.scores[:, :w]
+    return dataclasses.replace(b, scores=s)
