@@ -1,0 +1,140 @@
+/*
+ * topk_paged.h — C ABI of the GB300 (sm_103a) indexer top-k + paged slot library.
+ *
+ * Operation ("Serving GLM5.2 NVFP4 Agentic Workload with SGLang", section
+ * "Kernel Optimization > TopK-V2", Figs. 2-4 and the paragraphs after them):
+ * for every query row of fp32 indexer scores over the historical KV positions,
+ * select the top k (runtime k <= 2048) exactly in fp32 and translate each selected
+ * logical position into a physical indexer KV-cache slot through a paged block
+ * table, in one kernel. A planning kernel bins rows by length and builds a work
+ * list once per batch; the plan is reused by every select call (every indexer
+ * layer) of that batch.
+ *
+ * Readings of what the pages leave open (they define the exact result):
+ *   - order: position p ranks before q iff s(p) > s(q), or s(p) == s(q) and p < q;
+ *     IEEE equality, so -0.0 == +0.0; every NaN ranks below -inf;
+ *   - a row of valid length L yields min(k, L) entries; the remaining
+ *     k - min(k, L) entries of its output row are -1;
+ *   - slot(p) = block_table[t][p / page_size] * page_size + p % page_size with
+ *     t = row_to_table[r] (t = r when row_to_table is NULL), computed in 64 bits;
+ *   - the entries of a row are a set: their order inside the row is unspecified.
+ *
+ * Conventions for every call:
+ *   - "device" pointers point to memory of the current CUDA device; the caller owns
+ *     all memory. The library never allocates, frees or synchronizes, except
+ *     topk_read_status, which synchronizes `stream` to read the status word.
+ *   - work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream);
+ *   - a negative return value is a host-side argument error: nothing was enqueued.
+ *   - errors found on the device (bad lengths, bad table entries, a bounded wait
+ *     that expired) set bits in a sticky status word inside the workspace; read it
+ *     with topk_read_status. After a nonzero status, call topk_plan again before
+ *     the next select: the plan's counters may be left mid-call.
+ *   - one workspace serves one stream at a time: two calls that use the same
+ *     workspace must not run concurrently.
+ */
+#ifndef TOPK_PAGED_H
+#define TOPK_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* topk_stream_t; /* identical to cudaStream_t */
+
+/* Host-side return codes. */
+enum {
+  TOPK_OK = 0,
+  TOPK_ERR_NULL = -1,        /* a required pointer is NULL */
+  TOPK_ERR_ROWS = -2,        /* rows < 0 */
+  TOPK_ERR_K = -3,           /* k outside [1, TOPK_MAX_K] */
+  TOPK_ERR_PAGE_SIZE = -4,   /* page_size < 1 */
+  TOPK_ERR_LD = -5,          /* ld < max_len, or table_ld < 1 */
+  TOPK_ERR_WORKSPACE = -6,   /* workspace too small or not 256-byte aligned */
+  TOPK_ERR_MAX_LEN = -7,     /* max_len < 0 or above topk_max_row_len() */
+  TOPK_ERR_ALIGN = -8,       /* scores not 4-byte aligned / outputs not 4-byte aligned */
+  TOPK_ERR_CUDA = -9,        /* a CUDA runtime call failed (launch, attribute query) */
+  TOPK_ERR_DEVICE = -10,     /* current device cannot run the kernels (not sm_103) */
+  TOPK_ERR_CHUNK = -11       /* forced chunk size outside [16, topk_chunk_capacity()] */
+};
+
+/* Device status bits (sticky, OR-ed together; 0 = no error). */
+enum {
+  TOPK_STATUS_LEN = 1,            /* lens[r] outside [0, max_len]: row written as -1 */
+  TOPK_STATUS_TABLE_WIDTH = 2,    /* ceil(lens[r] / page_size) > table_ld: row written as -1 */
+  TOPK_STATUS_TABLE_ENTRY = 4,    /* a selected position's table entry is negative: that entry -1 */
+  TOPK_STATUS_SLOT_OVERFLOW = 8,  /* a slot exceeds INT32_MAX: that entry -1 */
+  TOPK_STATUS_TIMEOUT = 16,       /* a bounded cross-CTA wait expired: row contents undefined */
+  TOPK_STATUS_PLAN_MISMATCH = 32  /* lens/rows/max_len differ from the plan, or no plan: rows -1 */
+};
+
+#define TOPK_MAX_K 2048
+
+/* Bytes of workspace needed for a batch of `rows` rows whose lengths are at most
+ * `max_len`. Host only, pure (no CUDA call). Returns 0 for invalid arguments. */
+size_t topk_workspace_bytes(int rows, int max_len);
+
+/* Largest max_len supported on the current device (rows longer than this cannot be
+ * spread over the co-resident CTAs). Host only; queries the device. <= 0 on error. */
+int64_t topk_max_row_len(void);
+
+/* Elements one CTA keeps resident in shared memory (the largest chunk of a row one
+ * CTA processes). Host only, pure. */
+int topk_chunk_capacity(void);
+
+/* Planning kernel (one launch). Reads the device-resident lengths lens[rows] (int32,
+ * device) and writes the plan into `workspace` (device, 256-byte aligned, at least
+ * topk_workspace_bytes(rows, max_len) bytes): every row is binned by length into a
+ * path (copy-all for len <= k is decided later, per call), a single-CTA path whose
+ * row stays resident in one CTA's shared memory, or a multi-CTA path whose row is
+ * split into chunks processed by co-resident CTAs that combine their histograms
+ * through global memory. Also resets the workspace counters and the status word.
+ * The plan depends only on lens, rows and max_len; it is valid for every k and
+ * every score tensor. */
+int topk_plan(const int32_t* lens, int rows, int max_len, void* workspace,
+              size_t ws_bytes, topk_stream_t stream);
+
+/* topk_plan with a forced chunk size (elements per CTA, 16 <= chunk <=
+ * topk_chunk_capacity()): rows longer than `chunk` are split into ceil(len / chunk)
+ * CTAs. The result must not depend on the chunking; tests use this to drive the
+ * same rows through every path. chunk == 0 means the automatic choice. */
+int topk_plan_ex(const int32_t* lens, int rows, int max_len, int chunk, void* workspace,
+                 size_t ws_bytes, topk_stream_t stream);
+
+/* Select + page translation (one launch of a persistent, co-resident grid).
+ *   scores      device fp32 [rows, ld], row-major, 4-byte aligned; only the first
+ *               lens[r] entries of row r are read (in whole aligned 16-byte vectors)
+ *   ld          row stride in elements, ld >= max_len
+ *   lens        device int32 [rows]: must equal the lens given to topk_plan
+ *   k           1 <= k <= TOPK_MAX_K
+ *   block_table device int32 [n_tables, table_ld]: physical page ids
+ *   row_to_table device int32 [rows] (table row of each query row) or NULL (identity)
+ *   page_size   tokens per page, >= 1
+ *   out_slots   device int32 [rows, k]: selected slots, then -1 padding
+ *   out_pos     device int32 [rows, k] or NULL: the selected logical positions, in
+ *               the same order as out_slots, then -1 padding
+ *   workspace   the workspace holding a plan built for these lens/rows/max_len */
+int topk_select_paged(const float* scores, int64_t ld, const int32_t* lens, int rows,
+                      int max_len, int k, const int32_t* block_table, int64_t table_ld,
+                      const int32_t* row_to_table, int page_size, int32_t* out_slots,
+                      int32_t* out_pos, void* workspace, topk_stream_t stream);
+
+/* Synchronizes `stream`, then copies the device status word into *status. */
+int topk_read_status(const void* workspace, topk_stream_t stream, int* status);
+
+/* Enqueues a reset of the device status word to 0 on `stream`. */
+int topk_clear_status(void* workspace, topk_stream_t stream);
+
+/* Text for a host return code (negative) or a device status bit set (positive). */
+const char* topk_status_str(int code);
+
+/* Number of CTAs of the persistent select grid on the current device. */
+int topk_grid_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_PAGED_H */

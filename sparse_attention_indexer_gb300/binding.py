@@ -1,0 +1,172 @@
+"""Thin Python binding of the C ABI in include/topk_paged.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA library.
+Functions keep the C names and argument order; pointer arguments accept CUDA torch
+tensors (their data_ptr is passed) or plain integers, and `stream` accepts a
+torch.cuda.Stream, a raw handle or None (the current torch stream). If the library
+is missing this module raises; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtopk_paged.so")
+
+TOPK_MAX_K = 2048
+STATUS_LEN = 1
+STATUS_TABLE_WIDTH = 2
+STATUS_TABLE_ENTRY = 4
+STATUS_SLOT_OVERFLOW = 8
+STATUS_TIMEOUT = 16
+STATUS_PLAN_MISMATCH = 32
+
+EXPORTS = (
+    "topk_workspace_bytes", "topk_max_row_len", "topk_chunk_capacity", "topk_plan",
+    "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
+    "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
+)
+
+
+class TopKError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {code} ({status_str(code)})")
+        self.code = code
+
+
+_lib = None
+
+_c = ctypes
+_VP = _c.c_void_p
+_SIGS = {
+    "topk_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int]),
+    "topk_max_row_len": (_c.c_int64, []),
+    "topk_chunk_capacity": (_c.c_int, []),
+    "topk_grid_size": (_c.c_int, []),
+    "topk_plan": (_c.c_int, [_VP, _c.c_int, _c.c_int, _VP, _c.c_size_t, _VP]),
+    "topk_plan_ex": (_c.c_int, [_VP, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_size_t, _VP]),
+    "topk_select_paged": (_c.c_int, [_VP, _c.c_int64, _VP, _c.c_int, _c.c_int, _c.c_int, _VP,
+                                     _c.c_int64, _VP, _c.c_int, _VP, _VP, _VP, _VP]),
+    "topk_read_status": (_c.c_int, [_VP, _VP, _c.POINTER(_c.c_int)]),
+    "topk_clear_status": (_c.c_int, [_VP, _VP]),
+    "topk_status_str": (_c.c_char_p, [_c.c_int]),
+    "topk_plan_host": (_c.c_int, [_VP, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_size_t]),
+    "topk_layout_info": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int64), _c.c_int]),
+}
+
+
+def lib():
+    """Loads libtopk_paged.so (built by sparse_attention_indexer_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        if x.numel() > 0 and not x.is_cuda:
+            raise ValueError("device pointer argument must be a CUDA tensor")
+        return x.data_ptr() or None
+    return int(x)
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, torch.cuda.Stream):
+        return s.cuda_stream or None
+    return int(s) or None
+
+
+def _check(code: int, what: str) -> int:
+    if code < 0:
+        raise TopKError(code, what)
+    return code
+
+
+def status_str(code: int) -> str:
+    return lib().topk_status_str(int(code)).decode()
+
+
+topk_status_str = status_str
+
+
+def topk_workspace_bytes(rows: int, max_len: int) -> int:
+    return int(lib().topk_workspace_bytes(int(rows), int(max_len)))
+
+
+def topk_max_row_len() -> int:
+    return int(_check(lib().topk_max_row_len(), "topk_max_row_len"))
+
+
+def topk_chunk_capacity() -> int:
+    return int(lib().topk_chunk_capacity())
+
+
+def topk_grid_size() -> int:
+    return int(_check(lib().topk_grid_size(), "topk_grid_size"))
+
+
+def topk_plan(lens, rows: int, max_len: int, workspace, ws_bytes: int, stream=None) -> int:
+    return _check(lib().topk_plan(_ptr(lens), int(rows), int(max_len), _ptr(workspace),
+                                  int(ws_bytes), _stream(stream)), "topk_plan")
+
+
+def topk_plan_ex(lens, rows: int, max_len: int, chunk: int, workspace, ws_bytes: int,
+                 stream=None) -> int:
+    return _check(lib().topk_plan_ex(_ptr(lens), int(rows), int(max_len), int(chunk),
+                                     _ptr(workspace), int(ws_bytes), _stream(stream)),
+                  "topk_plan_ex")
+
+
+def topk_select_paged(scores, ld: int, lens, rows: int, max_len: int, k: int, block_table,
+                      table_ld: int, row_to_table, page_size: int, out_slots, out_pos,
+                      workspace, stream=None) -> int:
+    return _check(lib().topk_select_paged(
+        _ptr(scores), int(ld), _ptr(lens), int(rows), int(max_len), int(k), _ptr(block_table),
+        int(table_ld), _ptr(row_to_table), int(page_size), _ptr(out_slots), _ptr(out_pos),
+        _ptr(workspace), _stream(stream)), "topk_select_paged")
+
+
+def topk_read_status(workspace, stream=None) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().topk_read_status(_ptr(workspace), _stream(stream), ctypes.byref(v)),
+           "topk_read_status")
+    return int(v.value)
+
+
+def topk_clear_status(workspace, stream=None) -> int:
+    return _check(lib().topk_clear_status(_ptr(workspace), _stream(stream)), "topk_clear_status")
+
+
+def topk_plan_host(lens, rows: int, max_len: int, grid: int, chunk: int, image) -> int:
+    """Host reference of the planner writing into a host buffer (numpy uint8 array)."""
+    import numpy as np
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    return _check(lib().topk_plan_host(lens.ctypes.data_as(ctypes.c_void_p), int(rows),
+                                       int(max_len), int(grid), int(chunk),
+                                       image.ctypes.data_as(ctypes.c_void_p), int(image.nbytes)),
+                  "topk_plan_host")
+
+
+def topk_layout_info(rows: int):
+    arr = (ctypes.c_int64 * 11)()
+    _check(lib().topk_layout_info(int(rows), arr, 11), "topk_layout_info")
+    keys = ("max_grid", "max_waves", "chunk_cap", "header_bytes", "rowinfo", "singles",
+            "units", "groups", "threads", "group_cap", "list_cap")
+    return dict(zip(keys, [int(v) for v in arr]))

@@ -1,0 +1,213 @@
+// Shared definitions of the top-k + paged-slot kernels for GB300 (sm_103a):
+// tuning constants, the workspace layout written by the planner and read by the
+// select kernel, and small inline-PTX helpers (bulk copies, mbarriers, timers).
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/topk_paged.h"
+
+namespace topk {
+
+// ---------------------------------------------------------------- constants
+constexpr int kThreads = 512;              // threads per select CTA (16 warps)
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxGrid = 1024;             // largest persistent grid the plan describes
+constexpr int kMaxWaves = 64;              // waves of multi-CTA groups in one plan
+constexpr int kMaxGroups = 512;            // multi-CTA rows with group state in one plan
+constexpr int kChunkCap = 48128;           // elements one CTA keeps resident in smem
+constexpr int kChunkAlign = 16;            // chunk boundaries are multiples of 16 elements
+constexpr int kMinAutoChunk = 2048;        // automatic plans never split finer than this
+constexpr int kPieceBytes = 16384;         // one bulk copy (and one mbarrier) per piece
+constexpr int kBufFloats = kChunkCap + 8;  // resident buffer incl. alignment slack
+constexpr int kPieces = (kBufFloats * 4 + kPieceBytes - 1) / kPieceBytes;
+constexpr int kBins0 = 4096;               // coarse histogram (12-bit digit)
+constexpr int kLevelBits = 12;             // in-place refinement digit width
+constexpr int kListCap = 2048;             // single-CTA compact candidate list
+constexpr int kGroupCap = 4096;            // multi-CTA compact candidate list (global)
+constexpr int kListBins = 256;             // digit width 8 for list refinement
+constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
+constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // bounded waits: 200 ms
+
+// ---------------------------------------------------------------- workspace
+// All offsets are multiples of 256 bytes.
+struct Header {
+  uint32_t magic;
+  int32_t rows;
+  int32_t max_len;
+  int32_t grid;
+  int32_t chunk;        // chunk target chosen by the planner (elements)
+  int32_t waves;        // waves of the static multi-CTA unit table
+  int32_t n_single;     // rows processed by one CTA (dynamically claimed)
+  int32_t n_multi;      // rows split over several CTAs
+  int32_t status;       // sticky device status bits (TOPK_STATUS_*)
+  int32_t plan_error;   // nonzero when the plan could not be built
+  int32_t pad0[6];
+  unsigned long long steal;  // single-row ticket counter (advances by n_single + grid per call)
+  int32_t pad1[46];
+};
+static_assert(sizeof(Header) == 256, "header size");
+
+struct RowInfo {
+  int32_t len;    // length the plan was built for
+  int32_t G;      // CTAs sharing the row (1 = single-CTA path)
+  int32_t group;  // group-state index for G > 1, else -1
+  int32_t pad;
+};
+
+// Per multi-CTA row: counters reset by the row's last CTA of every call.
+struct GroupState {
+  uint32_t bar;        // spin-barrier arrivals during one call
+  uint32_t fin;        // end-of-row arrivals; advances by G per call (never reset)
+  uint32_t out_ctr;    // output entries reserved so far
+  uint32_t cand_ctr;   // compact candidates gathered so far
+  uint32_t and_key;    // AND of boundary keys (reset to ~0)
+  uint32_t or_key;     // OR of boundary keys (reset to 0)
+  uint32_t levels;     // refinement levels used (their histograms need clearing)
+  uint32_t pad[57];
+  uint32_t tie_cnt[kMaxGrid];
+  uint32_t hist0[kBins0];
+  uint32_t hlev[3][1 << kLevelBits];
+  uint32_t cand_key[kGroupCap];
+  uint32_t cand_pos[kGroupCap];
+};
+static_assert(sizeof(GroupState) % 256 == 0, "group state alignment");
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t header, rowinfo, singles, units, groups, total;
+  int ngroups;
+};
+
+__host__ __device__ inline Layout make_layout(int rows) {
+  Layout l;
+  l.ngroups = rows < kMaxGroups ? rows : kMaxGroups;
+  l.header = 0;
+  l.rowinfo = align256(sizeof(Header));
+  l.singles = l.rowinfo + align256(sizeof(RowInfo) * (size_t)(rows > 0 ? rows : 1));
+  l.units = l.singles + align256(sizeof(int32_t) * (size_t)(rows > 0 ? rows : 1));
+  l.groups = l.units + align256(sizeof(int32_t) * (size_t)kMaxWaves * kMaxGrid);
+  l.total = l.groups + sizeof(GroupState) * (size_t)l.ngroups;
+  return l;
+}
+
+// Unit table entry: row * kMaxGrid + rank, or -1.
+__host__ __device__ inline int32_t pack_unit(int row, int rank) { return row * kMaxGrid + rank; }
+
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Chunk of `rank` among G CTAs of a row of length L: [begin, end).
+__host__ __device__ inline void chunk_range(int L, int G, int rank, int* begin, int* end) {
+  int64_t c = ceil_div64(L, G);
+  c = ceil_div64(c, kChunkAlign) * kChunkAlign;
+  int64_t b = (int64_t)rank * c;
+  int64_t e = b + c;
+  if (b > L) b = L;
+  if (e > L) e = L;
+  *begin = (int)b;
+  *end = (int)e;
+}
+
+// Arguments of one select launch (see topk_select_paged in include/topk_paged.h).
+struct SelectParams {
+  const float* scores;
+  int64_t ld;
+  const int32_t* lens;
+  int rows;
+  int max_len;
+  int k;
+  const int32_t* table;
+  int64_t table_ld;
+  const int32_t* row_to_table;
+  int page_size;
+  int32_t* out_slots;
+  int32_t* out_pos;
+  char* ws;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
+}
+
+// Bulk (non-tensor) copy global -> shared, completion signalled on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete, for at most kWaitNs. Returns false
+// on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
+
+#endif  // __CUDACC__
+
+}  // namespace topk

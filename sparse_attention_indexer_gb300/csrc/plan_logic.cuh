@@ -1,0 +1,95 @@
+// Planning decisions shared by the device planning kernel and its host reference.
+//
+// "Serving GLM5.2 NVFP4 Agentic Workload with SGLang", "Kernel Optimization >
+// TopK-V2": a planning kernel picks the cutoff between the short-row paths and the
+// multi-CTA path from the batch's length distribution, and builds a work list for a
+// persistent grid; the plan is built once per forward and reused by every layer.
+//
+// Here the cutoff is a chunk size c (elements per CTA): rows with len <= c run on one
+// CTA (their row stays resident in that CTA's shared memory); longer rows are split
+// into G = ceil(len / c) CTAs that combine histograms through global memory. c starts
+// at ceil(total / grid) so the whole batch is spread evenly over the co-resident grid,
+// and grows while the multi-CTA groups do not fit one wave of the grid.
+#pragma once
+
+#include "common.cuh"
+
+namespace topk {
+
+struct PlanStats {
+  int64_t slots;  // sum of G over multi-CTA rows
+  int n_multi;    // rows with G >= 2
+  int max_g;      // largest G
+};
+
+__host__ __device__ inline int round_chunk(int64_t c) {
+  c = ceil_div64(c, kChunkAlign) * kChunkAlign;
+  if (c < kChunkAlign) c = kChunkAlign;
+  if (c > kChunkCap) c = kChunkCap;
+  return (int)c;
+}
+
+__host__ __device__ inline int valid_len(int32_t L, int max_len) {
+  return (L >= 0 && L <= max_len) ? L : 0;
+}
+
+__host__ __device__ inline int row_groups(int L, int c) {
+  return L > c ? (int)ceil_div64(L, c) : 1;
+}
+
+__host__ __device__ inline int initial_chunk(int64_t total, int grid, int forced) {
+  if (forced > 0) return round_chunk(forced);
+  int64_t c = grid > 0 ? ceil_div64(total, grid) : total;
+  if (c < kMinAutoChunk) c = kMinAutoChunk;
+  return round_chunk(c);
+}
+
+// Packs multi-CTA groups (in the given order) into waves of `grid` CTAs. A group never
+// straddles two waves. If `units` is non-null, writes unit ids at
+// units[wave * kMaxGrid + cta]. Returns the number of waves used.
+__host__ __device__ inline int pack_waves(const int32_t* multi_rows, const int32_t* multi_g,
+                                          int n_multi, int grid, int32_t* units) {
+  int64_t cursor = 0;
+  for (int i = 0; i < n_multi; ++i) {
+    const int G = multi_g[i];
+    if ((cursor % grid) + G > grid) cursor = ceil_div64(cursor, grid) * grid;
+    if (units) {
+      for (int j = 0; j < G; ++j) {
+        const int64_t s = cursor + j;
+        const int w = (int)(s / grid), cta = (int)(s % grid);
+        if (w < kMaxWaves) units[(int64_t)w * kMaxGrid + cta] = pack_unit(multi_rows[i], j);
+      }
+    }
+    cursor += G;
+  }
+  return (int)ceil_div64(cursor, grid);
+}
+
+// Decides whether chunk c is acceptable; if not, returns the next chunk to try
+// (> c), or -1 when no chunk works.
+__host__ __device__ inline int next_chunk(int c, const PlanStats& s, int waves, int grid,
+                                          bool forced, int ngroups) {
+  const bool hard_ok = s.max_g <= grid && s.n_multi <= ngroups && waves <= kMaxWaves;
+  const bool soft_ok = forced || s.slots <= grid;
+  if (hard_ok && soft_ok) return c;
+  if (c >= kChunkCap) return hard_ok ? c : -1;
+  int64_t nc = c + kChunkAlign;
+  if (!soft_ok && grid > 0) {
+    const int64_t scaled = ceil_div64((int64_t)c * s.slots, grid);
+    if (scaled > nc) nc = scaled;
+  }
+  if (!hard_ok && 2 * (int64_t)c > nc) nc = 2 * (int64_t)c;
+  return round_chunk(nc);
+}
+
+// Bucket of a single-CTA row for the longest-first claim order.
+__host__ __device__ inline int len_bucket(int L) {
+  int b = 0;
+  while (L > 1 && b < 31) {
+    L >>= 1;
+    ++b;
+  }
+  return b;
+}
+
+}  // namespace topk

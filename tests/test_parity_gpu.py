@@ -1,0 +1,277 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, bit-exact.
+
+Each GPU row is sorted by (score desc, position asc) and compared element by element
+with the oracle's positions and slots; padding must be -1 and the output buffers'
+guard canaries untouched. Covers every synthetic workload at full size, every k of
+the tie-heavy tiny rows, path forcing (the same rows through many chunkings), plan
+reuse, unaligned row strides, the error statuses and CUDA-graph replay.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import _checks as C
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from sparse_attention_indexer_gb300 import PagedTopK, binding as B  # noqa: E402
+from tests._gpu import compare_with_oracle, run_gpu, to_dev  # noqa: E402
+
+
+def test_library_loaded_and_device_supported():
+    assert B.topk_grid_size() > 0
+    assert B.topk_max_row_len() >= 1_000_006
+
+
+def test_pr1_ref():
+    b = W.pr1()
+    slots, pos, st = run_gpu(b)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, pos)
+
+
+@pytest.mark.parametrize("page_size", [64, 8])
+def test_tiny_rows_every_k(page_size):
+    for b in W.tiny_rows(page_size=page_size):
+        slots, pos, st = run_gpu(b)
+        assert st == 0
+        compare_with_oracle(b, b.k, slots, pos)
+
+
+def test_verify_80k():
+    b = W.verify_80k()
+    slots, pos, st = run_gpu(b)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, pos)
+
+
+def test_verify_1m():
+    b = W.verify_1m()
+    slots, pos, st = run_gpu(b)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, pos)
+
+
+def test_mixed_decode():
+    b = W.mixed_decode()
+    slots, pos, st = run_gpu(b)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, pos)
+
+
+def test_adversarial_all_k():
+    b = W.adversarial()
+    dev = to_dev(b)
+    core = PagedTopK(b.rows, b.max_len)
+    core.plan(dev[1])
+    for k in b.ks:
+        slots, pos, st = run_gpu(b, k=k, plan=core, dev_inputs=dev)
+        assert st == 0
+        compare_with_oracle(b, k, slots, pos)
+
+
+def _subset(b, rows):
+    return dataclasses.replace(b, scores=b.scores[rows].copy(), lens=b.lens[rows].copy(),
+                               block_table=b.block_table if b.row_to_table is not None
+                               else b.block_table[rows].copy(),
+                               row_to_table=None if b.row_to_table is None
+                               else b.row_to_table[rows].copy())
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 256, 1024, 5000, 0, 48128])
+def test_path_forcing_same_result(chunk):
+    """The result must not depend on how rows are split over CTAs."""
+    adv = _subset(W.adversarial(rows=48, max_len=20000), np.arange(48))
+    mixed = _subset(W.mixed_decode(), np.arange(6))
+    for b in (adv, mixed):
+        if chunk and chunk < 1024 and b is mixed:
+            continue  # would exceed the grid for 200K rows
+        for k in (1, 64, 2048):
+            slots, pos, st = run_gpu(b, k=k, chunk=chunk)
+            assert st == 0, B.status_str(st)
+            compare_with_oracle(b, k, slots, pos)
+
+
+def test_forced_multi_cta_on_ties():
+    """Tie-heavy rows forced onto many CTAs: all-equal, +/-0, fp16 grid, -inf tails."""
+    rng = np.random.default_rng(11)
+    L = 30000
+    rows = []
+    rows.append(np.full(L, 2.5, np.float32))
+    rows.append(np.where(np.arange(L) % 3 == 0, np.float32(-0.0), np.float32(0.0)))
+    rows.append(rng.standard_normal(L).astype(np.float16).astype(np.float32))
+    x = rng.standard_normal(L).astype(np.float32)
+    x[100:] = -np.inf
+    rows.append(x)
+    rows.append(rng.integers(-3, 4, L).astype(np.float32))
+    y = np.full(L, np.nan, np.float32)
+    y[::7] = -np.inf
+    rows.append(y)
+    s = np.stack(rows)
+    lens = np.full(len(rows), L, np.int32)
+    tab = np.stack([rng.permutation(-(-L // 64)).astype(np.int32) for _ in rows])
+    b = W.Batch("ties", s, lens, L, 2048, tab, None, 64)
+    for chunk in (0, 64, 1000, 4096):
+        for k in (1, 7, 2048):
+            slots, pos, st = run_gpu(b, k=k, chunk=chunk)
+            assert st == 0
+            compare_with_oracle(b, k, slots, pos)
+
+
+def test_special_values():
+    rng = np.random.default_rng(5)
+    L = 9000
+    vals = [np.float32(v) for v in (np.inf, -np.inf, 0.0, -0.0, 1e-40, -1e-40, 3.4e38,
+                                    -3.4e38, 65504.0, 70000.0, 2.0 ** -20, np.nan)]
+    rows = []
+    for i in range(8):
+        x = rng.choice(np.array(vals, np.float32), size=L)
+        x[rng.random(L) < 0.5] = rng.standard_normal(int((rng.random(L) < 0.5).sum()) or 1)[0]
+        rows.append(x.astype(np.float32))
+    s = np.stack(rows)
+    lens = np.array([L, L - 1, L - 2, L - 3, 5000, 2049, 2048, 1], np.int32)
+    tab = np.stack([rng.permutation(-(-L // 64)).astype(np.int32) for _ in rows])
+    b = W.Batch("special", s, lens, L, 2048, tab, None, 64)
+    for chunk in (0, 256):
+        for k in (1, 2, 2048):
+            slots, pos, st = run_gpu(b, k=k, chunk=chunk)
+            assert st == 0
+            compare_with_oracle(b, k, slots, pos)
+
+
+def test_unaligned_row_stride():
+    b = W.verify_80k()
+    b = W.with_ld(_subset(b, np.arange(3)), b.max_len)  # ld = 80006: rows start unaligned
+    assert b.ld % 4 != 0
+    slots, pos, st = run_gpu(b)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, pos)
+    m = _subset(W.mixed_decode(), np.arange(5))
+    m = W.with_ld(m, m.max_len + 3)
+    for chunk in (0, 4096):
+        slots, pos, st = run_gpu(m, chunk=chunk)
+        assert st == 0
+        compare_with_oracle(m, m.k, slots, pos)
+
+
+def test_plan_reuse_and_repeat():
+    """One plan serves many calls (new scores, new k); counters are left clean."""
+    b = W.verify_80k()
+    scores, lens, table, r2t = to_dev(b)
+    core = PagedTopK(b.rows, b.max_len)
+    core.plan(lens)
+    first = None
+    for it in range(4):
+        for k in (2048, 100, 1):
+            slots, pos, st = run_gpu(b, k=k, plan=core, dev_inputs=(scores, lens, table, r2t))
+            assert st == 0
+            if k == 2048:
+                if first is None:
+                    compare_with_oracle(b, k, slots, pos)
+                    first = np.sort(slots, axis=1)
+                else:
+                    assert np.array_equal(np.sort(slots, axis=1), first)
+    # new scores, same plan
+    b2 = dataclasses.replace(b, scores=W.verify_80k(seed=99).scores)
+    s2 = torch.from_numpy(b2.scores).cuda()
+    slots, pos, st = run_gpu(b2, plan=core, dev_inputs=(s2, lens, table, r2t))
+    assert st == 0
+    compare_with_oracle(b2, b2.k, slots, pos)
+
+
+def test_slots_only_output():
+    b = W.mixed_decode()
+    slots, _, st = run_gpu(b, with_pos=False)
+    assert st == 0
+    compare_with_oracle(b, b.k, slots, None)
+
+
+def test_device_plan_matches_host_reference():
+    from tests.test_plan_host import parse_plan
+    for b in (W.verify_80k(), W.verify_1m(), W.mixed_decode(), W.adversarial()):
+        lens = torch.from_numpy(b.lens).cuda()
+        core = PagedTopK(b.rows, b.max_len)
+        core.plan(lens)
+        img_dev = core.workspace.cpu().numpy()
+        img_host = np.zeros_like(img_dev)
+        B.topk_plan_host(b.lens, b.rows, b.max_len, B.topk_grid_size(), 0, img_host)
+        hd, rd, sd, ud, info = parse_plan(img_dev, b.rows)
+        hh, rh, sh, uh, _ = parse_plan(img_host, b.rows)
+        assert hd == hh
+        assert np.array_equal(rd, rh)
+        assert np.array_equal(sd[:hh["n_single"]], sh[:hh["n_single"]])
+        nw = hh["waves"] * info["max_grid"]
+        assert np.array_equal(ud[:nw], uh[:nw])
+
+
+def test_status_errors():
+    rng = np.random.default_rng(2)
+    L = 6000
+    s = rng.standard_normal((5, L)).astype(np.float32)
+    tab = np.stack([rng.permutation(L // 64 + 1).astype(np.int32) for _ in range(5)])
+    lens = np.array([L, L, L, L, L], np.int32)
+    # row 1: negative table entry on a page holding selected positions
+    s[1, 64:128] = 50.0
+    tab[1, 1] = -3
+    # row 2: slot overflow
+    s[2, 0:64] = 50.0
+    tab[2, 0] = 2 ** 30
+    b = W.Batch("errs", s, lens, L, 16, tab, None, 64)
+    slots, pos, st = run_gpu(b)
+    assert st == (B.STATUS_TABLE_ENTRY | B.STATUS_SLOT_OVERFLOW), B.status_str(st)
+    ref = oracle.topk_batch(b, threads=1)
+    assert ref[2] == 4 | 8
+    for r in range(5):
+        gp, gs = C.canonical(s[r], L, pos[r], slots[r], b.k)
+        assert np.array_equal(gp, ref[1][r]) and np.array_equal(gs, ref[0][r])
+    # length above max_len and table too narrow: those rows all -1
+    b2 = W.Batch("errs2", s[:3].copy(), np.array([L, L + 1, L], np.int32), L, 16,
+                 tab[:3, :50].copy(), None, 64)
+    slots, pos, st = run_gpu(b2)
+    assert st & B.STATUS_LEN and st & B.STATUS_TABLE_WIDTH
+    assert np.all(slots == -1) and np.all(pos == -1)
+
+
+def test_plan_mismatch_is_reported():
+    b = W.pr1()
+    scores, lens, table, r2t = to_dev(b)
+    core = PagedTopK(b.rows, b.max_len)
+    core.plan(lens)
+    other = lens.clone()
+    other[0] = 100
+    out = torch.empty((b.rows, b.k), dtype=torch.int32, device="cuda")
+    core.select(scores, other, b.k, table, b.page_size, r2t, out_slots=out)
+    st = core.status()
+    assert st & B.STATUS_PLAN_MISMATCH
+    assert torch.all(out[0] == -1)
+    core.clear_status()
+    assert core.status() == 0
+
+
+def test_cuda_graph_replay():
+    b = W.verify_80k()
+    scores, lens, table, r2t = to_dev(b)
+    core = PagedTopK(b.rows, b.max_len)
+    out = torch.empty((b.rows, b.k), dtype=torch.int32, device="cuda")
+    pos = torch.empty((b.rows, b.k), dtype=torch.int32, device="cuda")
+    core.plan(lens)
+    core.select(scores, lens, b.k, table, b.page_size, r2t, out_slots=out, out_pos=pos)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        core.plan(lens)
+        core.select(scores, lens, b.k, table, b.page_size, r2t, out_slots=out, out_pos=pos)
+    for _ in range(3):
+        out.fill_(-5)
+        g.replay()
+    torch.cuda.synchronize()
+    assert core.status() == 0
+    compare_with_oracle(b, b.k, out.cpu().numpy(), pos.cpu().numpy())

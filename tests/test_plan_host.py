@@ -1,0 +1,213 @@
+"""Planner logic and the C ABI, checked on the CPU (no GPU needed).
+
+The library's host reference of the planner (topk_plan_host) runs the same decisions
+as the planning kernel; these tests check the plans it builds for every workload
+against the invariants the select kernel relies on. They also check that the library
+loads and exports every entry point declared in include/topk_paged.h, and that host
+argument checks reject bad calls before anything is enqueued.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+S = pytest.importorskip("sparse_attention_indexer_gb300")
+B = S.binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib_or_skip():
+    if not os.path.exists(B.LIB_PATH):
+        pytest.skip("library not built")
+    return B.lib()
+
+
+def header_exports():
+    src = open(os.path.join(ROOT, "include", "topk_paged.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(topk_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = _lib_or_skip()
+    names = header_exports()
+    assert "topk_select_paged" in names and "topk_plan" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/topk_paged.h but not exported"
+    assert set(names) <= set(B.EXPORTS), set(names) - set(B.EXPORTS)
+
+
+def parse_plan(image, rows):
+    info = B.topk_layout_info(rows)
+    h = image[:256].view(np.int32)
+    hdr = dict(magic=int(h.view(np.uint32)[0]), rows=int(h[1]), max_len=int(h[2]), grid=int(h[3]),
+               chunk=int(h[4]), waves=int(h[5]), n_single=int(h[6]), n_multi=int(h[7]),
+               status=int(h[8]), plan_error=int(h[9]))
+    ri = image[info["rowinfo"]:info["rowinfo"] + 16 * rows].view(np.int32).reshape(rows, 4)
+    singles = image[info["singles"]:info["singles"] + 4 * rows].view(np.int32)
+    units = image[info["units"]:info["groups"]].view(np.int32)
+    return hdr, ri, singles, units, info
+
+
+def chunk_range(L, G, rank):
+    c = -(-L // G)
+    c = -(-c // 16) * 16
+    b = min(rank * c, L)
+    e = min(b + c, L) if rank * c <= L else L
+    return b, min(rank * c + c, L) if rank * c < L else L
+
+
+def host_plan(lens, max_len, grid, chunk=0):
+    rows = len(lens)
+    n = B.topk_workspace_bytes(rows, max_len)
+    image = np.zeros(n, dtype=np.uint8)
+    B.topk_plan_host(np.asarray(lens, np.int32), rows, max_len, grid, chunk, image)
+    return parse_plan(image, rows)
+
+
+def check_plan(lens, max_len, grid, chunk=0):
+    _lib_or_skip()
+    hdr, ri, singles, units, info = host_plan(lens, max_len, grid, chunk)
+    rows = len(lens)
+    assert hdr["magic"] == 0x54504B32 and hdr["rows"] == rows and hdr["grid"] == grid
+    assert hdr["plan_error"] == 0
+    cap = info["chunk_cap"]
+    maxg = info["max_grid"]
+    waves = hdr["waves"]
+    assert waves <= info["max_waves"]
+    seen = {}
+    for w in range(waves):
+        row_units = units[w * maxg:(w + 1) * maxg]
+        assert np.all(row_units[grid:] == -1) or waves == 0
+        for cta in range(grid):
+            u = int(row_units[cta])
+            if u < 0:
+                continue
+            r, rank = divmod(u, maxg)
+            assert (r, rank) not in seen, "unit assigned twice"
+            seen[(r, rank)] = (w, cta)
+    n_multi = 0
+    for r in range(rows):
+        L = int(lens[r])
+        Lv = L if 0 <= L <= max_len else 0
+        G = int(ri[r, 1])
+        assert int(ri[r, 0]) == L
+        if G > 1:
+            n_multi += 1
+            assert 0 <= int(ri[r, 2]) < info["max_grid"]
+            ws = {seen[(r, k)][0] for k in range(G)}
+            assert len(ws) == 1, "a multi-CTA row spans several waves"
+            ctas = {seen[(r, k)][1] for k in range(G)}
+            assert len(ctas) == G
+            covered = 0
+            for k in range(G):
+                c = -(-Lv // G)
+                c = -(-c // 16) * 16
+                b, e = min(k * c, Lv), min(k * c + c, Lv)
+                assert e - b <= cap
+                assert b == covered or e == b
+                covered = max(covered, e)
+            assert covered == Lv
+        else:
+            assert Lv <= cap
+            assert int(ri[r, 2]) == -1
+    assert n_multi == hdr["n_multi"]
+    assert len(seen) == sum(int(ri[r, 1]) for r in range(rows) if int(ri[r, 1]) > 1)
+    single_rows = [r for r in range(rows) if int(ri[r, 1]) == 1]
+    assert hdr["n_single"] == len(single_rows)
+    sl = [int(x) for x in singles[:hdr["n_single"]]]
+    assert sorted(sl) == single_rows
+    # longest bucket first
+    buckets = [int(np.floor(np.log2(max(1, lens[r] if 0 <= lens[r] <= max_len else 0) or 1)))
+               for r in sl]
+    assert buckets == sorted(buckets, reverse=True)
+    return hdr, ri
+
+
+@pytest.mark.parametrize("grid", [152, 148, 132])
+def test_plan_verify_configs_fit_one_wave(grid):
+    for b in (W.verify_80k(), W.verify_1m()):
+        hdr, ri = check_plan(b.lens, b.max_len, grid)
+        need = sum(-(-int(l) // B.topk_chunk_capacity()) for l in b.lens)
+        if need <= grid:  # one wave whenever the rows can fit the grid at all
+            assert hdr["waves"] == 1
+            assert int(ri[:, 1].sum()) <= grid
+
+
+def test_plan_80k_spreads_rows_over_the_grid():
+    b = W.verify_80k()
+    hdr, ri = check_plan(b.lens, b.max_len, 152)
+    assert all(int(g) >= 16 for g in ri[:, 1])
+
+
+def test_plan_all_workloads():
+    for b in [W.pr1(), W.mixed_decode(), W.adversarial()] + W.tiny_rows()[:3]:
+        check_plan(b.lens, b.max_len, 152)
+
+
+@pytest.mark.parametrize("chunk", [16, 64, 1000, 4096, 48128])
+def test_plan_forced_chunks(chunk):
+    b = W.mixed_decode()
+    if chunk < 4096:
+        lens = np.minimum(b.lens, 40000).astype(np.int32)
+        check_plan(lens[:8], 40000, 152, chunk)
+    else:
+        check_plan(b.lens, b.max_len, 152, chunk)
+
+
+def test_plan_degenerate_lengths():
+    check_plan(np.array([0, 0, 0], np.int32), 100, 152)
+    check_plan(np.array([-5, 101, 50], np.int32), 100, 152)  # invalid lengths become single rows
+    check_plan(np.array([], np.int32).reshape(0), 100, 152)
+    rng = np.random.default_rng(3)
+    lens = rng.integers(0, 300_000, size=400).astype(np.int32)
+    check_plan(lens, 300_000, 152)
+
+
+def test_plan_reports_too_many_long_rows():
+    """More rows longer than one CTA's capacity than there are group states: the plan
+    is marked failed (the select call then reports a plan mismatch, rows -1)."""
+    _lib_or_skip()
+    lens = np.full(600, 100_000, np.int32)
+    hdr, *_ = host_plan(lens, 100_000, 152)
+    assert hdr["plan_error"] == 1 and hdr["status"] == 32
+
+
+def test_plan_many_waves():
+    lens = np.full(40, 1_000_000, np.int32)
+    hdr, ri = check_plan(lens, 1_000_000, 152)
+    assert hdr["waves"] > 1
+
+
+def test_host_argument_errors():
+    _lib_or_skip()
+    assert B.topk_workspace_bytes(-1, 10) == 0
+    img = np.zeros(B.topk_workspace_bytes(2, 10), np.uint8)
+    with pytest.raises(B.TopKError):
+        B.topk_plan_host(np.array([1, 2], np.int32), 2, 10, 152, 8, img)  # chunk < 16
+    with pytest.raises(B.TopKError):
+        B.topk_plan_host(np.array([1, 2], np.int32), 2, 10, 0, 0, img)
+    with pytest.raises(B.TopKError):
+        B.topk_plan_host(np.array([1, 2], np.int32), 2, 10, 152, 0, img[:100])
+    lib = B.lib()
+    # select: argument checks happen before any CUDA call
+    assert lib.topk_select_paged(None, 10, None, 1, 10, 0, None, 1, None, 64, None, None, 256,
+                                 None) == -3   # k
+    assert lib.topk_select_paged(None, 10, None, 1, 10, 4, None, 1, None, 0, None, None, 256,
+                                 None) == -4   # page size
+    assert lib.topk_select_paged(None, 5, None, 1, 10, 4, None, 1, None, 64, None, None, 256,
+                                 None) == -5   # ld < max_len
+    assert lib.topk_select_paged(None, 10, None, 1, 10, 4, None, 1, None, 64, None, None, None,
+                                 None) == -1   # workspace
+    assert lib.topk_select_paged(None, 10, None, -1, 10, 4, None, 1, None, 64, None, None, 256,
+                                 None) == -2   # rows
+    assert lib.topk_select_paged(None, 10, None, 0, 10, 4, None, 1, None, 64, None, None, 256,
+                                 None) == 0    # empty batch: nothing to do
+    assert lib.topk_select_paged(4, 10, 4, 1, 10, 4, 4, 1, None, 64, 4, None, 100, None) == -6
+    assert lib.topk_select_paged(2, 10, 4, 1, 10, 4, 4, 1, None, 64, 4, None, 256, None) == -8
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -11, 1, 16, 3):
+        assert B.status_str(code)
