@@ -15,7 +15,7 @@ from typing import Optional
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtopk_paged.so")
+LIB_PATH = os.environ.get("TOPK_PAGED_LIB") or os.path.join(_PKG, "libtopk_paged.so")
 
 TOPK_MAX_K = 2048
 STATUS_LEN = 1
@@ -165,8 +165,8 @@ def topk_plan_host(lens, rows: int, max_len: int, grid: int, chunk: int, image) 
 
 
 def topk_layout_info(rows: int):
-    arr = (ctypes.c_int64 * 11)()
-    _check(lib().topk_layout_info(int(rows), arr, 11), "topk_layout_info")
+    arr = (ctypes.c_int64 * 12)()
+    _check(lib().topk_layout_info(int(rows), arr, 12), "topk_layout_info")
     keys = ("max_grid", "max_waves", "chunk_cap", "header_bytes", "rowinfo", "singles",
-            "units", "groups", "threads", "group_cap", "list_cap")
+            "first_single", "units", "groups", "threads", "group_cap", "list_cap")
     return dict(zip(keys, [int(v) for v in arr]))

@@ -40,18 +40,24 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          trace: bool = False) -> str:
+    """trace=True builds libtopk_paged_trace.so with the phase timer stamps compiled in
+    (exports topk_trace_select / topk_trace_plan); the default build has none."""
+    bdir = os.path.join(BUILD, "trace") if trace else BUILD
+    lib = LIB.replace(".so", "_trace.so") if trace else LIB
+    defs = ["-DTOPK_TRACE"] if trace else []
+    os.makedirs(bdir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "topk_paged.h")]
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or ptxas_info or _stale(o, [s] + hdrs):
             extra = ["-Xptxas", "-v"] if ptxas_info else []
-            jobs.append([nvcc()] + _flags(extra) + ["-c", s, "-o", o])
+            jobs.append([nvcc()] + _flags(extra + defs) + ["-c", s, "-o", o])
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             futs = [ex.submit(subprocess.run, j, capture_output=True, text=True) for j in jobs]
@@ -61,16 +67,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     sys.stderr.write(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed:\n{' '.join(j)}\n{r.stdout}\n{r.stderr}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                trace="--trace" in sys.argv))

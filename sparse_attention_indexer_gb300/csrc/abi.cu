@@ -210,16 +210,25 @@ int topk_plan_host(const int32_t* lens, int rows, int max_len, int grid, int chu
 }
 
 // Layout constants of the workspace and kernels, for tools and tests:
-// [0] kMaxGrid, [1] kMaxWaves, [2] kChunkCap, [3] header bytes, [4] row-info offset,
-// [5] singles offset, [6] units offset, [7] groups offset (all for `rows` rows),
-// [8] threads per CTA, [9] kGroupCap, [10] kListCap.
+// [0] kMaxGrid, [1] kMaxWaves, [2] kChunkCap, [3] header bytes, then byte offsets for
+// `rows` rows of [4] row info, [5] single rows, [6] first-single table, [7] unit
+// table, [8] group states; [9] threads per CTA, [10] kGroupCap, [11] kListCap.
 int topk_layout_info(int rows, int64_t* out, int n) {
   if (!out || rows < 0) return TOPK_ERR_NULL;
   const Layout l = make_layout(rows);
-  const int64_t v[11] = {kMaxGrid,          kMaxWaves,        kChunkCap,        (int64_t)sizeof(Header),
-                         (int64_t)l.rowinfo, (int64_t)l.singles, (int64_t)l.units, (int64_t)l.groups,
-                         kThreads,          kGroupCap,        kListCap};
-  for (int i = 0; i < n && i < 11; ++i) out[i] = v[i];
+  const int64_t v[12] = {kMaxGrid,
+                         kMaxWaves,
+                         kChunkCap,
+                         (int64_t)sizeof(Header),
+                         (int64_t)l.rowinfo,
+                         (int64_t)l.singles,
+                         (int64_t)l.first_single,
+                         (int64_t)l.units,
+                         (int64_t)l.groups,
+                         kThreads,
+                         kGroupCap,
+                         kListCap};
+  for (int i = 0; i < n && i < 12; ++i) out[i] = v[i];
   return TOPK_OK;
 }
 

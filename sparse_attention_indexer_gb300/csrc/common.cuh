@@ -3,6 +3,7 @@
 // select kernel, and small inline-PTX helpers (bulk copies, mbarriers, timers).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 #include "../../include/topk_paged.h"
@@ -13,7 +14,7 @@ namespace topk {
 constexpr int kThreads = 512;              // threads per select CTA (16 warps)
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxGrid = 1024;             // largest persistent grid the plan describes
-constexpr int kMaxWaves = 64;              // waves of multi-CTA groups in one plan
+constexpr int kMaxWaves = 16;              // waves of multi-CTA groups in one plan
 constexpr int kMaxGroups = 512;            // multi-CTA rows with group state in one plan
 constexpr int kChunkCap = 48128;           // elements one CTA keeps resident in smem
 constexpr int kChunkAlign = 16;            // chunk boundaries are multiples of 16 elements
@@ -23,7 +24,8 @@ constexpr int kBufFloats = kChunkCap + 8;  // resident buffer incl. alignment sl
 constexpr int kPieces = (kBufFloats * 4 + kPieceBytes - 1) / kPieceBytes;
 constexpr int kBins0 = 4096;               // coarse histogram (12-bit digit)
 constexpr int kLevelBits = 12;             // in-place refinement digit width
-constexpr int kListCap = 2048;             // single-CTA compact candidate list
+constexpr int kListCap = 1024;             // single-CTA compact candidate list (smem)
+constexpr int kRankMax = 192;              // boundary sets up to this size: rank counting
 constexpr int kGroupCap = 4096;            // multi-CTA compact candidate list (global)
 constexpr int kListBins = 256;             // digit width 8 for list refinement
 constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
@@ -38,15 +40,23 @@ struct Header {
   int32_t grid;
   int32_t chunk;        // chunk target chosen by the planner (elements)
   int32_t waves;        // waves of the static multi-CTA unit table
-  int32_t n_single;     // rows processed by one CTA (dynamically claimed)
+  int32_t n_single;     // rows processed by one CTA
   int32_t n_multi;      // rows split over several CTAs
   int32_t status;       // sticky device status bits (TOPK_STATUS_*)
   int32_t plan_error;   // nonzero when the plan could not be built
-  int32_t pad0[6];
-  unsigned long long steal;  // single-row ticket counter (advances by n_single + grid per call)
-  int32_t pad1[46];
+  int32_t n_implicit;   // single rows handed out statically (one per idle CTA)
+  int32_t dyn_period;   // claims of the ticket counter per call
+  int32_t pad0[4];
+  unsigned long long steal;  // single-row ticket counter (advances by dyn_period per call)
+  int32_t pad1[14];
+  // First expired bounded wait (written once per plan, for diagnosis): kind
+  // (1 = row barrier, 2 = piece copy), row, rank, barrier sequence, observed count,
+  // target count, CTA index, unit wave-or-single marker.
+  int32_t diag[8];
+  int32_t pad2[24];
 };
 static_assert(sizeof(Header) == 256, "header size");
+static_assert(offsetof(Header, diag) == 128, "diagnostic record offset");
 
 struct RowInfo {
   int32_t len;    // length the plan was built for
@@ -55,14 +65,21 @@ struct RowInfo {
   int32_t pad;
 };
 
+// One CTA's share of a row: positions [s0, s0 + n) of row `row` (plan length len),
+// chunk `rank` of G; `group` indexes the row's GroupState (-1 when G == 1).
+struct __align__(16) UnitDesc {
+  int32_t row, s0, n, len;
+  int32_t rank, G, group, pad;
+};
+
 // Per multi-CTA row: counters reset by the row's last CTA of every call.
 struct GroupState {
   uint32_t bar;        // spin-barrier arrivals during one call
-  uint32_t fin;        // end-of-row arrivals; advances by G per call (never reset)
-  uint32_t out_ctr;    // output entries reserved so far
-  uint32_t cand_ctr;   // compact candidates gathered so far
-  uint32_t and_key;    // AND of boundary keys (reset to ~0)
-  uint32_t or_key;     // OR of boundary keys (reset to 0)
+  uint32_t fin;        // end-of-row arrivals during one call
+  uint32_t out_ctr;    // output entries reserved so far     (low word of one u64)
+  uint32_t cand_ctr;   // compact candidates gathered so far (high word)
+  uint32_t and_key;    // ~AND of boundary keys (stored inverted: reset value 0)
+  uint32_t or_key;     // OR of boundary keys
   uint32_t levels;     // refinement levels used (their histograms need clearing)
   uint32_t pad[57];
   uint32_t tie_cnt[kMaxGrid];
@@ -76,24 +93,23 @@ static_assert(sizeof(GroupState) % 256 == 0, "group state alignment");
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t header, rowinfo, singles, units, groups, total;
+  size_t header, rowinfo, singles, first_single, units, groups, total;
   int ngroups;
 };
 
 __host__ __device__ inline Layout make_layout(int rows) {
   Layout l;
+  const size_t r = (size_t)(rows > 0 ? rows : 1);
   l.ngroups = rows < kMaxGroups ? rows : kMaxGroups;
   l.header = 0;
   l.rowinfo = align256(sizeof(Header));
-  l.singles = l.rowinfo + align256(sizeof(RowInfo) * (size_t)(rows > 0 ? rows : 1));
-  l.units = l.singles + align256(sizeof(int32_t) * (size_t)(rows > 0 ? rows : 1));
-  l.groups = l.units + align256(sizeof(int32_t) * (size_t)kMaxWaves * kMaxGrid);
+  l.singles = l.rowinfo + align256(sizeof(RowInfo) * r);
+  l.first_single = l.singles + align256(sizeof(int32_t) * 2 * r);
+  l.units = l.first_single + align256(sizeof(int32_t) * (size_t)kMaxGrid);
+  l.groups = l.units + align256(sizeof(UnitDesc) * (size_t)kMaxWaves * kMaxGrid);
   l.total = l.groups + sizeof(GroupState) * (size_t)l.ngroups;
   return l;
 }
-
-// Unit table entry: row * kMaxGrid + rank, or -1.
-__host__ __device__ inline int32_t pack_unit(int row, int rank) { return row * kMaxGrid + rank; }
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -209,5 +225,18 @@ __device__ __forceinline__ void red_add_u32(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
 
 #endif  // __CUDACC__
+
+// Optional phase trace (compiled in only with -DTOPK_TRACE): thread 0 of each CTA
+// stamps %globaltimer at fixed points into a per-translation-unit device array.
+#if defined(TOPK_TRACE) && defined(__CUDACC__)
+#define TOPK_MARK(arr, slot)                                                       \
+  do {                                                                             \
+    if (threadIdx.x == 0 && (slot) < 16) arr[blockIdx.x * 16 + (slot)] = global_timer_ns(); \
+  } while (0)
+#else
+#define TOPK_MARK(arr, slot) \
+  do {                       \
+  } while (0)
+#endif
 
 }  // namespace topk

@@ -33,8 +33,9 @@ __host__ __device__ inline int valid_len(int32_t L, int max_len) {
   return (L >= 0 && L <= max_len) ? L : 0;
 }
 
+// CTAs for a row of (valid) length L at chunk c (32-bit: L < 2^31, c <= kChunkCap).
 __host__ __device__ inline int row_groups(int L, int c) {
-  return L > c ? (int)ceil_div64(L, c) : 1;
+  return L > c ? (int)(((uint32_t)L + (uint32_t)c - 1u) / (uint32_t)c) : 1;
 }
 
 __host__ __device__ inline int initial_chunk(int64_t total, int grid, int forced) {
@@ -44,25 +45,24 @@ __host__ __device__ inline int initial_chunk(int64_t total, int grid, int forced
   return round_chunk(c);
 }
 
-// Packs multi-CTA groups (in the given order) into waves of `grid` CTAs. A group never
-// straddles two waves. If `units` is non-null, writes unit ids at
-// units[wave * kMaxGrid + cta]. Returns the number of waves used.
-__host__ __device__ inline int pack_waves(const int32_t* multi_rows, const int32_t* multi_g,
-                                          int n_multi, int grid, int32_t* units) {
-  int64_t cursor = 0;
-  for (int i = 0; i < n_multi; ++i) {
-    const int G = multi_g[i];
-    if ((cursor % grid) + G > grid) cursor = ceil_div64(cursor, grid) * grid;
-    if (units) {
-      for (int j = 0; j < G; ++j) {
-        const int64_t s = cursor + j;
-        const int w = (int)(s / grid), cta = (int)(s % grid);
-        if (w < kMaxWaves) units[(int64_t)w * kMaxGrid + cta] = pack_unit(multi_rows[i], j);
-      }
+// Packs multi-CTA groups (sizes g[0..n), in order) into waves of `grid` CTAs; a group
+// never straddles two waves. Writes each group's wave and first CTA when the output
+// arrays are non-null. Returns the number of waves.
+__host__ __device__ inline int pack_waves(const int32_t* g, int n, int grid, int32_t* wave,
+                                          int32_t* first_cta) {
+  int w = 0, used = 0;
+  for (int i = 0; i < n; ++i) {
+    if (used + g[i] > grid) {
+      ++w;
+      used = 0;
     }
-    cursor += G;
+    if (wave) {
+      wave[i] = w;
+      first_cta[i] = used;
+    }
+    used += g[i];
   }
-  return (int)ceil_div64(cursor, grid);
+  return n > 0 ? w + 1 : 0;
 }
 
 // Decides whether chunk c is acceptable; if not, returns the next chunk to try
@@ -90,6 +90,22 @@ __host__ __device__ inline int len_bucket(int L) {
     ++b;
   }
   return b;
+}
+
+// The unit of chunk `rank` of a row split over G CTAs.
+__host__ __device__ inline UnitDesc make_unit(int row, int L, int rank, int G, int group) {
+  UnitDesc u;
+  int b, e;
+  chunk_range(L, G, rank, &b, &e);
+  u.row = row;
+  u.s0 = b;
+  u.n = e - b;
+  u.len = L;
+  u.rank = rank;
+  u.G = G;
+  u.group = group;
+  u.pad = 0;
+  return u;
 }
 
 }  // namespace topk

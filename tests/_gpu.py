@@ -35,6 +35,9 @@ def run_gpu(b, k=None, chunk=0, with_pos=True, guard=64, plan=None, dev_inputs=N
     out_p = pbuf[guard:guard + n].view(rows, k) if with_pos else None
     core.select(scores, lens, k, table, b.page_size, r2t, out_slots=out_s, out_pos=out_p)
     status = core.status()
+    if status & 16:
+        diag = core.workspace[128:160].cpu().numpy().view(np.int32)
+        print(f"timeout record (kind,row,rank,seq,seen,target,cta): {diag.tolist()}")
     sb = sbuf.cpu().numpy()
     assert np.all(sb[:guard] == -777) and np.all(sb[guard + n:] == -777), "slot canary overwritten"
     pos = None

@@ -195,20 +195,24 @@ def test_slots_only_output():
 
 def test_device_plan_matches_host_reference():
     from tests.test_plan_host import parse_plan
+    grid = B.topk_grid_size()
     for b in (W.verify_80k(), W.verify_1m(), W.mixed_decode(), W.adversarial()):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
         img_dev = core.workspace.cpu().numpy()
         img_host = np.zeros_like(img_dev)
-        B.topk_plan_host(b.lens, b.rows, b.max_len, B.topk_grid_size(), 0, img_host)
-        hd, rd, sd, ud, info = parse_plan(img_dev, b.rows)
-        hh, rh, sh, uh, _ = parse_plan(img_host, b.rows)
+        B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img_host)
+        hd, rd, sd, (fd, ud), info = parse_plan(img_dev, b.rows)
+        hh, rh, sh, (fh, uh), _ = parse_plan(img_host, b.rows)
         assert hd == hh
         assert np.array_equal(rd, rh)
         assert np.array_equal(sd[:hh["n_single"]], sh[:hh["n_single"]])
+        assert np.array_equal(fd[:grid], fh[:grid])
         nw = hh["waves"] * info["max_grid"]
-        assert np.array_equal(ud[:nw], uh[:nw])
+        used = uh[:nw, 0] >= 0
+        assert np.array_equal(ud[:nw, 0] >= 0, used)
+        assert np.array_equal(ud[:nw][used, :7], uh[:nw][used, :7])
 
 
 def test_status_errors():

@@ -46,19 +46,13 @@ def parse_plan(image, rows):
     h = image[:256].view(np.int32)
     hdr = dict(magic=int(h.view(np.uint32)[0]), rows=int(h[1]), max_len=int(h[2]), grid=int(h[3]),
                chunk=int(h[4]), waves=int(h[5]), n_single=int(h[6]), n_multi=int(h[7]),
-               status=int(h[8]), plan_error=int(h[9]))
+               status=int(h[8]), plan_error=int(h[9]), n_implicit=int(h[10]),
+               dyn_period=int(h[11]))
     ri = image[info["rowinfo"]:info["rowinfo"] + 16 * rows].view(np.int32).reshape(rows, 4)
-    singles = image[info["singles"]:info["singles"] + 4 * rows].view(np.int32)
-    units = image[info["units"]:info["groups"]].view(np.int32)
-    return hdr, ri, singles, units, info
-
-
-def chunk_range(L, G, rank):
-    c = -(-L // G)
-    c = -(-c // 16) * 16
-    b = min(rank * c, L)
-    e = min(b + c, L) if rank * c <= L else L
-    return b, min(rank * c + c, L) if rank * c < L else L
+    singles = image[info["singles"]:info["singles"] + 8 * rows].view(np.int32).reshape(rows, 2)
+    first = image[info["first_single"]:info["first_single"] + 4 * info["max_grid"]].view(np.int32)
+    units = image[info["units"]:info["groups"]].view(np.int32).reshape(-1, 8)
+    return hdr, ri, singles, (first, units), info
 
 
 def host_plan(lens, max_len, grid, chunk=0):
@@ -70,8 +64,13 @@ def host_plan(lens, max_len, grid, chunk=0):
 
 
 def check_plan(lens, max_len, grid, chunk=0):
+    """Invariants the select kernel relies on: each multi-CTA row's chunks cover it
+    exactly, sit in one wave on distinct CTAs and fit one CTA's shared memory; single
+    rows fit one CTA; every single row is listed once, longest bucket first; each
+    CTA without static work gets at most one single row up front; the ticket period
+    counts one claim per remaining single row plus one failing claim per CTA."""
     _lib_or_skip()
-    hdr, ri, singles, units, info = host_plan(lens, max_len, grid, chunk)
+    hdr, ri, singles, (first, units), info = host_plan(lens, max_len, grid, chunk)
     rows = len(lens)
     assert hdr["magic"] == 0x54504B32 and hdr["rows"] == rows and hdr["grid"] == grid
     assert hdr["plan_error"] == 0
@@ -80,16 +79,17 @@ def check_plan(lens, max_len, grid, chunk=0):
     waves = hdr["waves"]
     assert waves <= info["max_waves"]
     seen = {}
+    busy = np.zeros(grid, bool)
     for w in range(waves):
-        row_units = units[w * maxg:(w + 1) * maxg]
-        assert np.all(row_units[grid:] == -1) or waves == 0
-        for cta in range(grid):
-            u = int(row_units[cta])
-            if u < 0:
+        for cta in range(maxg):
+            u = units[w * maxg + cta]
+            if u[0] < 0:
                 continue
-            r, rank = divmod(u, maxg)
-            assert (r, rank) not in seen, "unit assigned twice"
-            seen[(r, rank)] = (w, cta)
+            assert cta < grid
+            row, s0, n, L, rank, G, group = (int(v) for v in u[:7])
+            assert (row, rank) not in seen, "unit assigned twice"
+            seen[(row, rank)] = (w, cta, s0, n, L, G, group)
+            busy[cta] = True
     n_multi = 0
     for r in range(rows):
         L = int(lens[r])
@@ -98,19 +98,16 @@ def check_plan(lens, max_len, grid, chunk=0):
         assert int(ri[r, 0]) == L
         if G > 1:
             n_multi += 1
-            assert 0 <= int(ri[r, 2]) < info["max_grid"]
-            ws = {seen[(r, k)][0] for k in range(G)}
-            assert len(ws) == 1, "a multi-CTA row spans several waves"
-            ctas = {seen[(r, k)][1] for k in range(G)}
-            assert len(ctas) == G
+            assert 0 <= int(ri[r, 2]) < hdr["n_multi"]
+            parts = [seen[(r, k)] for k in range(G)]
+            assert len({p[0] for p in parts}) == 1, "a multi-CTA row spans several waves"
+            assert len({p[1] for p in parts}) == G
             covered = 0
-            for k in range(G):
-                c = -(-Lv // G)
-                c = -(-c // 16) * 16
-                b, e = min(k * c, Lv), min(k * c + c, Lv)
-                assert e - b <= cap
-                assert b == covered or e == b
-                covered = max(covered, e)
+            for k, (w, cta, s0, n, Lu, Gu, grp) in enumerate(parts):
+                assert Lu == L and Gu == G and grp == int(ri[r, 2])
+                assert 0 <= n <= cap and s0 % 16 == 0
+                assert s0 == covered or n == 0
+                covered = max(covered, s0 + n)
             assert covered == Lv
         else:
             assert Lv <= cap
@@ -119,12 +116,19 @@ def check_plan(lens, max_len, grid, chunk=0):
     assert len(seen) == sum(int(ri[r, 1]) for r in range(rows) if int(ri[r, 1]) > 1)
     single_rows = [r for r in range(rows) if int(ri[r, 1]) == 1]
     assert hdr["n_single"] == len(single_rows)
-    sl = [int(x) for x in singles[:hdr["n_single"]]]
+    sl = [int(x) for x in singles[:hdr["n_single"], 0]]
     assert sorted(sl) == single_rows
-    # longest bucket first
+    assert [int(x) for x in singles[:hdr["n_single"], 1]] == [int(lens[r]) for r in sl]
     buckets = [int(np.floor(np.log2(max(1, lens[r] if 0 <= lens[r] <= max_len else 0) or 1)))
                for r in sl]
     assert buckets == sorted(buckets, reverse=True)
+    free = [c for c in range(grid) if not busy[c]]
+    exp_first = [-1] * grid
+    for i, c in enumerate(free[:hdr["n_single"]]):
+        exp_first[c] = i
+    assert [int(x) for x in first[:grid]] == exp_first
+    assert hdr["n_implicit"] == min(len(free), hdr["n_single"])
+    assert hdr["dyn_period"] == hdr["n_single"] - hdr["n_implicit"] + grid
     return hdr, ri
 
 
