@@ -5,8 +5,9 @@ the select + page-table launch, inputs resident in HBM. The headline workload is
 bs=1 MTP target-verify batch at 1M ISL (7 rows x 1,000,000..1,000,006 fp32 scores,
 k=2048, 64-token pages); the 80K ISL verify batch is reported beside it.
 
-The L2 (129 MB) is flushed by a 256 MiB write between timed steps, outside the
-timed events. Prints one JSON line (rank 0).
+Each timed step replays the step as one CUDA graph. The L2 (129 MB) is flushed before
+every timed step, outside the timed events (a 256 MiB write, then a 256 MiB read of
+another buffer). Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -137,7 +138,8 @@ def _dist():
 
 
 class _Batch:
-    """Device copies of one workload batch plus its plan object."""
+    """Device copies of one workload batch, its plan object and two CUDA graphs: the
+    whole step (plan + select) and select alone."""
 
     def __init__(self, b, dev):
         import torch
@@ -149,6 +151,8 @@ class _Batch:
         self.r2t = None if b.row_to_table is None else torch.from_numpy(b.row_to_table).to(dev)
         self.core = PagedTopK(b.rows, b.max_len, dev)
         self.out = torch.empty((b.rows, b.k), dtype=torch.int32, device=dev)
+        self.g_step = None
+        self.g_select = None
 
     def plan(self):
         self.core.plan(self.lens)
@@ -157,48 +161,55 @@ class _Batch:
         self.core.select(self.scores, self.lens, self.b.k, self.table, self.b.page_size,
                          self.r2t, out_slots=self.out)
 
+    def capture(self):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.plan()
+            self.select()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step, stream=s):
+            self.plan()
+            self.select()
+        self.g_select = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_select, stream=s):
+            self.select()
+        torch.cuda.synchronize()
 
-def _time_steps(bt, steps, flush, with_plan=True):
-    """Per-step CUDA-event times (ms) of plan+select and of select alone, L2 flushed
-    before every step (outside the events). Returns (step_ms[], select_ms[])."""
+
+class _Flush:
+    """Evicts the L2 between timed steps: writes one 256 MiB buffer, then reads another,
+    so no dirty line of the flush is left for the timed step to write back."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self, i):
+        import torch
+        self.w.fill_(i & 0xFF)
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+def _time(fn, steps, flush):
+    """Per-step CUDA-event times (ms) of fn(), L2 flushed before each (outside the events)."""
     import torch
     st = torch.cuda.current_stream()
-    e = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
     for i in range(steps):
         if flush is not None:
-            flush.fill_(i & 0xFF)
-        e[i][0].record(st)
-        if with_plan:
-            bt.plan()
-        e[i][1].record(st)
-        bt.select()
-        e[i][2].record(st)
+            flush(i)
+        ev[i][0].record(st)
+        fn()
+        ev[i][1].record(st)
     torch.cuda.synchronize()
-    step = [e[i][0].elapsed_time(e[i][2]) for i in range(steps)]
-    sel = [e[i][1].elapsed_time(e[i][2]) for i in range(steps)]
-    return step, sel
-
-
-def _graph_select_us(bt, reps=200):
-    """Select alone replayed from a CUDA graph, warm L2 (labelled as such)."""
-    import torch
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        bt.select()
-    torch.cuda.current_stream().wait_stream(s)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        bt.select()
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1000.0 / reps
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def _cpu_baseline(b, budget_s=10.0):
@@ -272,19 +283,22 @@ def run_ours(args):
     b80 = W.verify_80k()
     bt = _Batch(b1m, dev)
     bt80 = _Batch(b80, dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = _Flush(dev)
 
     # correctness guard: the timed path must report a clean status
-    bt.plan(); bt.select(); bt80.plan(); bt80.select()
+    for x in (bt, bt80):
+        x.plan()
+        x.select()
     torch.cuda.synchronize()
     for x in (bt, bt80):
         stt = x.core.status()
         if stt != 0:
             raise RuntimeError(f"device status {stt}: {Bd.status_str(stt)}")
+        x.capture()
 
     # warm-up (also brings the clocks up)
-    _time_steps(bt, max(args.warmup, 3), flush)
-    _time_steps(bt80, max(args.warmup, 3), flush)
+    for x in (bt, bt80):
+        _time(x.g_step.replay, max(args.warmup, 3), flush)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if n > 1:
@@ -293,7 +307,7 @@ def run_ours(args):
     if sampler:
         sampler.start()
     wall0 = time.perf_counter()
-    step_ms, sel_ms = _time_steps(bt, args.steps, flush)
+    step_ms = _time(bt.g_step.replay, args.steps, flush)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
@@ -309,17 +323,20 @@ def run_ours(args):
     score_bytes = 4 * int(b1m.lens.astype(np.int64).sum())
     value = n * score_bytes * args.steps / (total_ms / 1e3) / 1e9
     ms_step = total_ms / args.steps
+    nsec = min(args.steps, 300)
+    sel_ms = _time(bt.g_select.replay, nsec, flush)
     sel_avg_ms = float(np.mean(sel_ms))
     alg_bytes = b1m.algorithmic_bytes()
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (sel_avg_ms / 1e3) / 1e9
 
-    # secondary: 80K ISL latency
-    s80, sel80 = _time_steps(bt80, args.steps, flush)
-    # warm-L2 and graph-replay numbers (labelled)
-    w_step, w_sel = _time_steps(bt, min(args.steps, 200), None)
-    g_us = _graph_select_us(bt)
-    g80_us = _graph_select_us(bt80)
+    # secondary: 80K ISL latency (graph replay), eager calls, warm L2
+    s80 = _time(bt80.g_step.replay, nsec, flush)
+    sel80 = _time(bt80.g_select.replay, nsec, flush)
+    e_step = _time(lambda: (bt.plan(), bt.select()), min(nsec, 100), flush)
+    e_step80 = _time(lambda: (bt80.plan(), bt80.select()), min(nsec, 100), flush)
+    w_sel = _time(bt.g_select.replay, min(nsec, 100), None)
+    w_sel80 = _time(bt80.g_select.replay, min(nsec, 100), None)
 
     # end to end through the public API on pinned host buffers
     e2e = None
@@ -338,7 +355,7 @@ def run_ours(args):
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         tot = 0.0
         for i in range(ne):
-            flush.fill_(i & 0xFF)
+            flush(i)
             a.record(st)
             out_h = hp(sh, lh, th, rh, b1m.page_size)
             z.record(st)
@@ -368,14 +385,17 @@ def run_ours(args):
             "workload": "verify_1m: bs=1 MTP target verify at 1M ISL, 7 rows x "
                         "1,000,000..1,000,006 fp32 scores (N(0,1) + sin bias), k=2048, "
                         "page_size=64, one shuffled table of 15,626 pages",
-            "step": "topk_plan + topk_select_paged (2 launches), inputs resident in HBM",
-            "l2": "flushed between steps by a 256 MiB write (outside the timed events)",
+            "step": "topk_plan + topk_select_paged (2 kernels) replayed as one CUDA graph, "
+                    "inputs resident in HBM",
+            "l2": "flushed before every timed step (outside the events): 256 MiB write, "
+                  "then 256 MiB read of another buffer",
             "value_def": "score bytes (4 * sum(lens)) per step / mean step time, all ranks",
             "vs_baseline_def": "pages' TopK-V2 36.6 us at 1M ISL / our us per step "
                                "(other hardware: context only)",
             "parallelism": f"replicas x{n}",
         },
         "us_per_call": {
+            "note": "CUDA-graph replay, L2 flushed before each call unless marked warm",
             "verify_1m_plan_select": round(ms_step * 1e3, 2),
             "verify_1m_select": round(sel_avg_ms * 1e3, 2),
             "verify_1m_select_p10_p90": [round(float(np.percentile(sel_ms, 10)) * 1e3, 2),
@@ -385,8 +405,9 @@ def run_ours(args):
             "verify_80k_select_p10_p90": [round(float(np.percentile(sel80, 10)) * 1e3, 2),
                                           round(float(np.percentile(sel80, 90)) * 1e3, 2)],
             "verify_1m_select_warm_l2": round(float(np.mean(w_sel)) * 1e3, 2),
-            "verify_1m_select_graph_warm_l2": round(g_us, 2),
-            "verify_80k_select_graph_warm_l2": round(g80_us, 2),
+            "verify_80k_select_warm_l2": round(float(np.mean(w_sel80)) * 1e3, 2),
+            "verify_1m_plan_select_eager": round(float(np.mean(e_step)) * 1e3, 2),
+            "verify_80k_plan_select_eager": round(float(np.mean(e_step80)) * 1e3, 2),
             "pages_topk_v2": {"80k": PAGES_80K_US, "1m": PAGES_1M_US},
         },
         "roofline": {

@@ -26,6 +26,7 @@ constexpr int kBins0 = 4096;               // coarse histogram (12-bit digit)
 constexpr int kLevelBits = 12;             // in-place refinement digit width
 constexpr int kListCap = 1024;             // single-CTA compact candidate list (smem)
 constexpr int kRankMax = 192;              // boundary sets up to this size: rank counting
+constexpr int kRankOwnMax = 1024;          // multi-CTA rows: each CTA ranks its own candidates
 constexpr int kGroupCap = 4096;            // multi-CTA compact candidate list (global)
 constexpr int kListBins = 256;             // digit width 8 for list refinement
 constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
@@ -72,17 +73,18 @@ struct __align__(16) UnitDesc {
   int32_t rank, G, group, pad;
 };
 
-// Per multi-CTA row: counters reset by the row's last CTA of every call.
+// Per multi-CTA row. `bar` is a generation barrier counter: every CTA of the row
+// adds 1 per barrier, so it stays a multiple of G between barriers and is never
+// reset by the select kernel. The histograms are cleared by the CTAs that wrote
+// them once a later barrier shows every CTA has read them; the per-rank arrays are
+// overwritten by every call.
 struct GroupState {
-  uint32_t bar;        // spin-barrier arrivals during one call
-  uint32_t fin;        // end-of-row arrivals during one call
-  uint32_t out_ctr;    // output entries reserved so far     (low word of one u64)
-  uint32_t cand_ctr;   // compact candidates gathered so far (high word)
-  uint32_t and_key;    // ~AND of boundary keys (stored inverted: reset value 0)
-  uint32_t or_key;     // OR of boundary keys
-  uint32_t levels;     // refinement levels used (their histograms need clearing)
-  uint32_t pad[57];
-  uint32_t tie_cnt[kMaxGrid];
+  unsigned long long bar;  // barrier arrivals (generation = bar / G)
+  uint32_t and_key;        // ~AND of boundary keys (stored inverted: reset value 0)
+  uint32_t or_key;         // OR of boundary keys
+  uint32_t pad[60];
+  uint32_t cnt[kMaxGrid];      // per rank: staged emissions | candidates << 16
+  uint32_t tie_cnt[kMaxGrid];  // per rank: tied values (in-place refinement)
   uint32_t hist0[kBins0];
   uint32_t hlev[3][1 << kLevelBits];
   uint32_t cand_key[kGroupCap];
@@ -208,6 +210,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -231,7 +239,7 @@ __device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg
 #if defined(TOPK_TRACE) && defined(__CUDACC__)
 #define TOPK_MARK(arr, slot)                                                       \
   do {                                                                             \
-    if (threadIdx.x == 0 && (slot) < 16) arr[blockIdx.x * 16 + (slot)] = global_timer_ns(); \
+    if (threadIdx.x == 0 && (slot) < 32) arr[blockIdx.x * 32 + (slot)] = global_timer_ns(); \
   } while (0)
 #else
 #define TOPK_MARK(arr, slot) \

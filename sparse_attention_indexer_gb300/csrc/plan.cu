@@ -20,11 +20,12 @@ namespace topk {
 namespace {
 
 #ifdef TOPK_TRACE
-__device__ uint64_t g_plan_trace[kMaxGrid * 16];
+__device__ uint64_t g_plan_trace[kMaxGrid * 32];
 #endif
 
 constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kLensCache = 4096;  // batches up to this many rows plan from shared memory
 
 struct PlanSmem {
   long long red64[kPlanWarps];
@@ -36,6 +37,7 @@ struct PlanSmem {
   int32_t multi_cta[kMaxGroups];
   uint32_t busy[kMaxGrid / 32];  // CTAs with static units
   unsigned bucket_mask;
+  int32_t lens[kLensCache];
 };
 
 __device__ void block_stats(long long& a, int& b, int& c, PlanSmem& s) {
@@ -114,9 +116,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   __shared__ PlanSmem s;
   const int tid = threadIdx.x;
 
+  // Lengths are read many times below: keep them in shared memory when they fit.
+  const bool cached = rows <= kLensCache;
+  if (cached)
+    for (int r = tid; r < rows; r += kPlanThreads) s.lens[r] = lens[r];
+  __syncthreads();
+  const int32_t* L_ = cached ? s.lens : lens;
+
   long long total = 0;
   int dummy_b = 0, dummy_c = 0;
-  for (int r = tid; r < rows; r += kPlanThreads) total += valid_len(lens[r], max_len);
+  for (int r = tid; r < rows; r += kPlanThreads) total += valid_len(L_[r], max_len);
   block_stats(total, dummy_b, dummy_c, s);
   TOPK_MARK(g_plan_trace, 1);
 
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     long long slots = 0;
     int nm = 0, mg = 0;
     for (int r = tid; r < rows; r += kPlanThreads) {
-      const int G = row_groups(valid_len(lens[r], max_len), c);
+      const int G = row_groups(valid_len(L_[r], max_len), c);
       if (G > 1) {
         slots += G;
         nm += 1;
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       int base = 0;
       for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
         const int r = r0 + tid;
-        const int G = r < rows ? row_groups(valid_len(lens[r], max_len), c) : 1;
+        const int G = r < rows ? row_groups(valid_len(L_[r], max_len), c) : 1;
         int tot;
         const int off = block_scan(G > 1 ? 1 : 0, &tot, s);
         if (G > 1) {
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     for (int i = 0; i < st.n_multi; ++i) {
       const int G = s.multi_g[i];
       const int row = s.multi_rows[i];
-      const int L = valid_len(lens[row], max_len);
+      const int L = valid_len(L_[row], max_len);
       for (int j = tid; j < G; j += kPlanThreads) {
         const int cta = s.multi_cta[i] + j;
         units[(int64_t)s.multi_wave[i] * kMaxGrid + cta] = make_unit(row, L, j, G, i);
@@ -188,9 +197,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
   // Row info.
   for (int r = tid; r < rows; r += kPlanThreads) {
-    const int L = valid_len(lens[r], max_len);
+    const int L = valid_len(L_[r], max_len);
     RowInfo x;
-    x.len = lens[r];
+    x.len = L_[r];
     x.G = plan_error ? 1 : row_groups(L, c);
     x.group = -1;
     x.pad = 0;
@@ -205,7 +214,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   if (tid == 0) s.bucket_mask = 0u;
   __syncthreads();
   for (int r = tid; r < rows; r += kPlanThreads) {
-    const int L = valid_len(lens[r], max_len);
+    const int L = valid_len(L_[r], max_len);
     if (plan_error || row_groups(L, c) == 1) atomicOr(&s.bucket_mask, 1u << len_bucket(L));
   }
   __syncthreads();
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       bool take = false;
       int Lraw = 0;
       if (r < rows) {
-        Lraw = lens[r];
+        Lraw = L_[r];
         const int L = valid_len(Lraw, max_len);
         take = (plan_error || row_groups(L, c) == 1) && len_bucket(L) == b;
       }
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
 #ifdef TOPK_TRACE
 extern "C" int topk_trace_plan(uint64_t* host, int n) {
-  if (n > kMaxGrid * 16) n = kMaxGrid * 16;
+  if (n > kMaxGrid * 32) n = kMaxGrid * 32;
   return cudaMemcpyFromSymbol(host, g_plan_trace, sizeof(uint64_t) * n) == cudaSuccess ? 0 : -9;
 }
 #endif

@@ -29,7 +29,7 @@ namespace topk {
 namespace {
 
 #ifdef TOPK_TRACE
-__device__ uint64_t g_select_trace[kMaxGrid * 16];
+__device__ uint64_t g_select_trace[kMaxGrid * 32];
 // Per-CTA event log: (row + 1) << 44 | event << 40 | low 40 bits of %globaltimer.
 __device__ uint64_t g_select_log[kMaxGrid * 64];
 __device__ int g_select_log_n[kMaxGrid];
@@ -69,6 +69,7 @@ struct __align__(16) Smem {
   uint64_t mbar[kPieces];
   int wsum[kWarps];
   int wsum2[kWarps];
+  unsigned long long wsum64[kWarps];
   uint32_t wand[kWarps];
   uint32_t wor[kWarps];
   int bc[32];
@@ -205,6 +206,7 @@ __device__ void record_timeout(Header* h, int kind, int row, int rank, int seq, 
 
 struct Unit {
   int r, rank, G, L, kr, t, s0, n, head, nvec, npieces;
+  int blocal;  // lowest coarse bin this CTA published to the row histogram
   GroupState* gs;
   uint32_t bar_seq;  // barriers passed in this unit
 };
@@ -249,61 +251,105 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 }
 
 // Group barrier among the G CTAs of a row. All threads call it; a thread that wrote
-// row state to global memory (histogram reductions, candidates, counts) passes
+// row state to global memory (histogram reductions, counts, candidates) passes
 // wrote = true and fences its own writes first, so that they are performed before
-// thread 0 releases the arrival (a release by one thread does not order other
-// warps' writes still in flight). The waiting side acquires. Returns false if the
+// thread 0 arrives (an arrival by one thread does not order other warps' writes
+// still in flight). Generation barrier: the arrival returns the count before it,
+// and the barrier opens when the count reaches the next multiple of G, so the
+// counter never needs a reset. The waiting side acquires. Returns false if the
 // bounded wait expired (status set).
 __device__ bool group_barrier(Ctx& c, Unit& u, bool wrote) {
   if (wrote) __threadfence();
   __syncthreads();
   u.bar_seq += 1;
   if (threadIdx.x == 0) {
-    const uint32_t target = (uint32_t)u.G * u.bar_seq;
-    red_release_add_u32(&u.gs->bar, 1u);
-    bool ok = ld_acquire_u32(&u.gs->bar) >= target;
+    __threadfence();
+    const unsigned long long G = (unsigned long long)u.G;
+    const unsigned long long old = atomicAdd(&u.gs->bar, 1ull);
+    const unsigned long long target = (old / G + 1ull) * G;
+    bool ok = old + 1ull == target || ld_acquire_u64(&u.gs->bar) >= target;
     if (!ok) {
       const uint64_t t0 = global_timer_ns();
       while (true) {
-        if (ld_acquire_u32(&u.gs->bar) >= target) {
+        if (ld_acquire_u64(&u.gs->bar) >= target) {
           ok = true;
           break;
         }
         if (global_timer_ns() - t0 > kWaitNs) break;
       }
     }
+    __threadfence();
     c.s.bc[15] = ok ? 1 : 0;
     if (!ok) {
       set_status(c.h, TOPK_STATUS_TIMEOUT);
-      record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, (int)ld_acquire_u32(&u.gs->bar),
-                     (int)target);
+      record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, (int)(ld_acquire_u64(&u.gs->bar) % G),
+                     (int)G);
     }
   }
   __syncthreads();
   return c.s.bc[15] != 0;
 }
 
-// Finds bin b of a 4096-bin histogram (8 bins per thread, counts in v[]) with
-// above(b) < need <= above(b) + hist[b]; above(b) counts bins > b. Results land in
-// s.bc[0..2] = (b, above, eq). Requires 1 <= need <= total.
-__device__ void find_threshold(const uint32_t (&v)[8], int need, Smem& s) {
-  int sum = 0;
+// Exclusive prefix over ranks < u.rank of the per-rank words gs->cnt (two 16-bit
+// fields), published before the last barrier.
+__device__ int rank_prefix(Ctx& c, const Unit& u, const uint32_t* arr) {
+  int acc = 0;
+  for (int j = threadIdx.x; j < u.rank; j += kThreads) acc += (int)__ldcg(&arr[j]);
+  return block_sum(acc, c.s);
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_scan64(unsigned long long x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) sum += (int)v[j];
-  int total;
-  const int excl = block_excl_scan(sum, &total, s);
-  const int above_t = total - excl - sum;  // bins owned by higher threads
-  if (above_t < need && need <= above_t + sum) {
-    int cum = above_t;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+// Finds bin b of a 4096-bin histogram (8 bins per thread: row-wide counts g[], this
+// CTA's counts l[]) with above(b) < need <= above(b) + g[b], above(b) counting bins
+// > b. Writes s.bc[0..4] = (b, above, g[b], this CTA's count above b, l[b]) with one
+// scan of the packed (row, local) per-thread sums. Requires 1 <= need <= sum(g).
+__device__ void find_threshold(const uint32_t (&g)[8], const uint32_t (&l)[8], int need, Smem& s) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned long long gs = 0, ls = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    gs += g[j];
+    ls += l[j];
+  }
+  const unsigned long long v = (gs << 32) | ls;
+  const unsigned long long incl = warp_incl_scan64(v);
+  if (lane == 31) s.wsum64[w] = incl;
+  __syncthreads();
+  unsigned long long before = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) {
+    const unsigned long long x = s.wsum64[i];
+    if (i < w) before += x;
+    total += x;
+  }
+  const unsigned long long excl = before + incl - v;
+  // counts owned by higher threads
+  const long long g_above = (long long)(total >> 32) - (long long)(excl >> 32) - (long long)gs;
+  const long long l_above = (long long)(total & 0xFFFFFFFFull) - (long long)(excl & 0xFFFFFFFFull) -
+                            (long long)ls;
+  if (g_above < need && need <= g_above + (long long)gs) {
+    long long cg = g_above, cl = l_above;
 #pragma unroll
     for (int j = 7; j >= 0; --j) {
-      if (cum + (int)v[j] >= need) {
+      if (cg + (long long)g[j] >= need) {
         s.bc[0] = threadIdx.x * 8 + j;
-        s.bc[1] = cum;
-        s.bc[2] = (int)v[j];
+        s.bc[1] = (int)cg;
+        s.bc[2] = (int)g[j];
+        s.bc[3] = (int)cl;
+        s.bc[4] = (int)l[j];
         break;
       }
-      cum += (int)v[j];
+      cg += g[j];
+      cl += l[j];
     }
   }
   __syncthreads();
@@ -339,13 +385,12 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
   const int b0 = threadIdx.x * 8;
   load8(&s.u.hist[b0], loc);
   if (u.G > 1) {
-    // Own threshold bin: only meaningful when this chunk alone holds `need` values;
-    // then the row's threshold cannot lie below it. Otherwise every bin counts.
     int blocal = 0;
     if (sparse && local_n >= need) {
-      find_threshold(loc, need, s);
+      find_threshold(loc, loc, need, s);
       blocal = s.bc[0];
     }
+    u.blocal = blocal;
     bool wrote = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -364,29 +409,23 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
 #pragma unroll
     for (int j = 0; j < 8; ++j) glob[j] = loc[j];
   }
-  find_threshold(glob, need, s);
+  find_threshold(glob, loc, need, s);
   b = s.bc[0];
   above = s.bc[1];
   eq = s.bc[2];
-  int la = 0, le = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (b0 + j > b) la += (int)loc[j];
-    if (b0 + j == b) le = (int)loc[j];
-  }
-  if (b >= b0 && b < b0 + 8) s.bc[3] = le;
-  local_above = block_sum(la, s);  // its CTA barriers also publish bc[3]
-  local_eq = s.bc[3];
+  local_above = s.bc[3];
+  local_eq = s.bc[4];
   __syncthreads();
   return true;
 }
 
 // ------------------------------------------------------------- chunk loading
 
-// Thread 0 issues the bulk copies of the unit's chunk [s0, s0 + n) of row r.
-__device__ void issue_chunk(Ctx& c, Unit& u) {
-  Smem& s = c.s;
-  const SelectParams& P = c.p;
+// Geometry of the unit's chunk [s0, s0 + n) of row r in shared memory: the copy
+// covers the aligned 16-byte vectors holding the chunk; element 0 sits at float
+// index `head`.
+__device__ __forceinline__ uint32_t chunk_geometry(const SelectParams& P, Unit& u,
+                                                    const char** src_aligned) {
   const float* src = P.scores + (int64_t)u.r * P.ld + u.s0;
   const uintptr_t A = reinterpret_cast<uintptr_t>(src);
   const uintptr_t A0 = A & ~uintptr_t(15);
@@ -395,16 +434,26 @@ __device__ void issue_chunk(Ctx& c, Unit& u) {
   u.head = (int)((A - A0) >> 2);
   u.nvec = (int)(bytes >> 4);
   u.npieces = (int)((bytes + kPieceBytes - 1) / kPieceBytes);
-  if (threadIdx.x == 0) {
-    fence_proxy_async_smem();
-    for (int i = 0; i < u.npieces; ++i) {
-      const uint32_t off = (uint32_t)i * kPieceBytes;
-      const uint32_t sz = min((uint32_t)kPieceBytes, bytes - off);
-      mbar_arrive_expect_tx(&s.mbar[i], sz);
-      bulk_g2s(reinterpret_cast<char*>(s.buf) + off, reinterpret_cast<const char*>(A0) + off, sz,
-               &s.mbar[i]);
-    }
+  *src_aligned = reinterpret_cast<const char*>(A0);
+  return bytes;
+}
+
+// Bulk copies of the chunk, one per 16 KB piece, each completing on its mbarrier.
+// Called by one thread after the previous unit's shared-memory accesses completed.
+__device__ void issue_copies(Smem& s, const char* src, uint32_t bytes, int npieces) {
+  fence_proxy_async_smem();
+  for (int i = 0; i < npieces; ++i) {
+    const uint32_t off = (uint32_t)i * kPieceBytes;
+    const uint32_t sz = min((uint32_t)kPieceBytes, bytes - off);
+    mbar_arrive_expect_tx(&s.mbar[i], sz);
+    bulk_g2s(reinterpret_cast<char*>(s.buf) + off, src + off, sz, &s.mbar[i]);
   }
+}
+
+__device__ void issue_chunk(Ctx& c, Unit& u) {
+  const char* src;
+  const uint32_t bytes = chunk_geometry(c.p, u, &src);
+  if (threadIdx.x == 0) issue_copies(c.s, src, bytes, u.npieces);
 }
 
 __device__ __forceinline__ void wait_piece(Ctx& c, int i) {
@@ -426,76 +475,58 @@ __device__ void drain_chunk(Ctx& c, Unit& u) {
   __syncthreads();
 }
 
-// Adds a full float4's digits. A warp whose 128 values share one digit adds them
-// with one atomic (all-equal rows, -inf tails); otherwise one atomic per value.
-// All 32 lanes must call it.
-__device__ __forceinline__ void hist_add4(Smem& s, uint32_t d0, uint32_t d1, uint32_t d2,
-                                          uint32_t d3, bool full) {
-  const int lane = threadIdx.x & 31;
-  const bool uni = full && d0 == d1 && d1 == d2 && d2 == d3;
-  const uint32_t dl = __shfl_sync(0xffffffffu, d0, 0);
-  if (__all_sync(0xffffffffu, uni && d0 == dl)) {
-    if (lane == 0) atomicAdd(&s.u.hist[d0], 128u);
-  } else if (full) {
-    atomicAdd(&s.u.hist[d0], 1u);
-    atomicAdd(&s.u.hist[d1], 1u);
-    atomicAdd(&s.u.hist[d2], 1u);
-    atomicAdd(&s.u.hist[d3], 1u);
-  }
-}
-
-// Waits for the pieces as they land and builds the coarse histogram of the chunk in
-// s.u.hist (zeroed by the caller before the CTA barrier that precedes this call).
+// Builds the coarse histogram of the chunk in s.u.hist (zeroed by the caller before
+// the CTA barrier that precedes this call) while the pieces land. Each thread walks
+// its vectors (stride kThreads) and waits on a piece's mbarrier only when it first
+// reaches a vector of that piece; no warp-synchronous step in the loop.
 __device__ void histogram_chunk(Ctx& c, Unit& u) {
   Smem& s = c.s;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   constexpr int kVecPerPiece = kPieceBytes / 16;
-  // Vectors [vfull0, vfull1) hold only chunk elements; the first and last vectors may
-  // be partial.
-  const int vfull0 = (u.head + 3) >> 2;
-  const int vfull1 = (u.head + u.n) >> 2;
+  int landed = 0;        // pieces this thread has seen complete
+  int landed_end = 0;    // vectors below this index have landed
 #ifdef TOPK_TRACE
   uint64_t waited = 0;
 #endif
-  for (int i = 0; i < u.npieces; ++i) {
+  auto ensure = [&](int v) {
+    while (v >= landed_end && landed < u.npieces) {
 #ifdef TOPK_TRACE
-    const uint64_t w0 = global_timer_ns();
+      const uint64_t w0 = global_timer_ns();
 #endif
-    wait_piece(c, i);
+      wait_piece(c, landed);
 #ifdef TOPK_TRACE
-    waited += global_timer_ns() - w0;
-    if (threadIdx.x == 0 && i == u.npieces - 1)
-      g_select_trace[blockIdx.x * 16 + 11] = global_timer_ns();
+      waited += global_timer_ns() - w0;
 #endif
-    const int vbeg = i * kVecPerPiece;
-    const int vend = min(vbeg + kVecPerPiece, u.nvec);
-    for (int vb = vbeg + warp * 32; vb < vend; vb += kThreads) {
-      const int v = vb + lane;
-      if (vb + 32 <= vend && vb >= vfull0 && vb + 32 <= vfull1) {
-        const float4 x = b4[v];
-        hist_add4(s, coarse_digit(x.x), coarse_digit(x.y), coarse_digit(x.z),
-                  coarse_digit(x.w), true);
-      } else {
-        const bool act = v < vend;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (act) x = b4[v];
-        const int e0 = 4 * v - u.head;
-        const bool full = act && e0 >= 0 && e0 + 3 < u.n;
-        const uint32_t d0 = coarse_digit(x.x), d1 = coarse_digit(x.y);
-        const uint32_t d2 = coarse_digit(x.z), d3 = coarse_digit(x.w);
-        hist_add4(s, d0, d1, d2, d3, full);
-        if (act && !full) {
-          if (e0 >= 0 && e0 < u.n) atomicAdd(&s.u.hist[d0], 1u);
-          if (e0 + 1 >= 0 && e0 + 1 < u.n) atomicAdd(&s.u.hist[d1], 1u);
-          if (e0 + 2 >= 0 && e0 + 2 < u.n) atomicAdd(&s.u.hist[d2], 1u);
-          if (e0 + 3 >= 0 && e0 + 3 < u.n) atomicAdd(&s.u.hist[d3], 1u);
-        }
-      }
+      ++landed;
+      landed_end += kVecPerPiece;
+    }
+  };
+  const int vfull0 = (u.head + 3) >> 2;  // first vector holding only chunk elements
+  const int vfull1 = (u.head + u.n) >> 2;
+  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+    ensure(v);
+    const float4 x = b4[v];
+    if (v >= vfull0 && v < vfull1) {
+      atomicAdd(&s.u.hist[coarse_digit(x.x)], 1u);
+      atomicAdd(&s.u.hist[coarse_digit(x.y)], 1u);
+      atomicAdd(&s.u.hist[coarse_digit(x.z)], 1u);
+      atomicAdd(&s.u.hist[coarse_digit(x.w)], 1u);
+    } else {  // first or last vector of the chunk
+      const int e0 = 4 * v - u.head;
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (e0 + j >= 0 && e0 + j < u.n) atomicAdd(&s.u.hist[coarse_digit(xs[j])], 1u);
     }
   }
+  // Every thread must observe every issued piece (the mbarrier phases advance once
+  // per unit), including pieces past its last vector.
+  ensure(u.nvec > 0 ? u.npieces * kVecPerPiece - 1 : -1);
 #ifdef TOPK_TRACE
-  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 16 + 10] = waited;
+  if (threadIdx.x == 0) {
+    g_select_trace[blockIdx.x * 32 + 10] = waited;
+    g_select_trace[blockIdx.x * 32 + 11] = global_timer_ns();
+  }
 #endif
   __syncthreads();
 }
@@ -504,17 +535,35 @@ __device__ void histogram_chunk(Ctx& c, Unit& u) {
 
 // Exact selection among n <= kRankMax candidates: candidate i is taken iff fewer
 // than `need` candidates rank before it (larger key, or equal key and smaller
-// position); it goes to output index base + its rank (deterministic order).
+// position); it goes to output index base + its rank (deterministic order). A group
+// of T lanes shares each candidate's comparisons.
 __device__ void rank_select_emit(Ctx& c, const Unit& u, const uint32_t* key, const uint32_t* pos,
                                  int n, int need, int base) {
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const uint32_t ki = key[i], pi = pos[i];
+  int T = 1;
+  while (T < 8 && n * (T * 2) <= kThreads) T *= 2;  // lanes per candidate (1..8)
+  const int sub = threadIdx.x & (T - 1);
+  for (int i0 = 0; i0 < n * T; i0 += kThreads) {
+    const int i = (i0 + threadIdx.x) / T;  // groups never straddle a warp (T divides 32)
+    const bool act = i < n;
+    const uint32_t ki = act ? key[i] : 0u, pi = act ? pos[i] : 0u;
     int rank = 0;
-    for (int j = 0; j < n; ++j) {
-      const uint32_t kj = key[j], pj = pos[j];
-      rank += (kj > ki || (kj == ki && pj < pi)) ? 1 : 0;
+    if (act) {
+      int j = sub;
+      for (; j + 3 * T < n; j += 4 * T) {
+        const uint32_t k0 = key[j], k1 = key[j + T], k2 = key[j + 2 * T], k3 = key[j + 3 * T];
+        const uint32_t p0 = pos[j], p1 = pos[j + T], p2 = pos[j + 2 * T], p3 = pos[j + 3 * T];
+        rank += (k0 > ki || (k0 == ki && p0 < pi)) ? 1 : 0;
+        rank += (k1 > ki || (k1 == ki && p1 < pi)) ? 1 : 0;
+        rank += (k2 > ki || (k2 == ki && p2 < pi)) ? 1 : 0;
+        rank += (k3 > ki || (k3 == ki && p3 < pi)) ? 1 : 0;
+      }
+      for (; j < n; j += T) {
+        const uint32_t kj = key[j], pj = pos[j];
+        rank += (kj > ki || (kj == ki && pj < pi)) ? 1 : 0;
+      }
     }
-    if (rank < need) emit(c, u, base + rank, (int)pi);
+    for (int o = 1; o < T; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (act && sub == 0 && rank < need) emit(c, u, base + rank, (int)pi);
   }
 }
 
@@ -627,14 +676,54 @@ __device__ void select_boundary(Ctx& c, const Unit& u, const uint32_t* key, cons
 
 // ------------------------------------------------------------- in-place fallback
 
+// Emits, in a fixed order (thread, then vector), every chunk value whose index e and
+// value x satisfy pred(e, x), at output indices base, base + 1, ... Two passes over
+// the resident chunk: count, CTA scan, write.
+template <class Pred>
+__device__ void emit_ordered(Ctx& c, const Unit& u, int base, Pred pred) {
+  const float4* b4 = reinterpret_cast<const float4*>(c.s.buf);
+  int cnt = 0;
+  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+    const float4 x = b4[v];
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e >= 0 && e < u.n && pred(e, xs[j])) ++cnt;
+    }
+  }
+  int total;
+  int o = base + block_excl_scan(cnt, &total, c.s);
+  if (cnt == 0) return;
+  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+    const float4 x = b4[v];
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e >= 0 && e < u.n && pred(e, xs[j])) emit(c, u, o++, u.s0 + e);
+    }
+  }
+}
+
 // Boundary bin too large for a compact list (massive ties): refine in place on the
 // full key, then take tied values in position order. fa/fo: AND/OR of the boundary
-// keys over the row. `need` values remain to be chosen among coarse digit b0.
-__device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int above0, uint32_t fa,
+// keys over the row; `need` values remain to be chosen among coarse digit b0, after
+// `emitted` row entries (all values above the threshold bin). For G > 1 every level
+// exchanges per-rank counts so that output offsets are deterministic, and each CTA
+// clears the level histogram once the next barrier shows it has been read.
+__device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, uint32_t fa,
                                 uint32_t fo, int local_eq0) {
   Smem& s = c.s;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
-  int emitted = above0;  // G == 1: running output index
+  bool reset_and_or = u.G > 1;  // cleared by rank 0 after the next barrier
+  auto passed_barrier = [&]() {
+    if (reset_and_or && u.rank == 0 && threadIdx.x == 0) {
+      u.gs->and_key = 0u;
+      u.gs->or_key = 0u;
+    }
+    reset_and_or = false;
+  };
   uint32_t pmask = 0u, pval = 0u;
   int local_tie = local_eq0;
   bool done = false;
@@ -662,38 +751,29 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int above0, u
         }
       }
       __syncthreads();
-      if (u.G > 1 && threadIdx.x == 0) u.gs->levels = (uint32_t)(lev + 1);
       int bl, abl, eql, lal, lel;
       if (!reduce_and_find(c, u, u.G > 1 ? u.gs->hlev[lev] : nullptr, need, 0, false, bl, abl,
                            eql, lal, lel))
         return false;
+      if (u.G > 1) passed_barrier();
       need -= abl;
       const bool take = (eql == need);
-      if (threadIdx.x == 0) {
-        const int cnt = lal + (take ? lel : 0);
-        s.bc[7] = u.G > 1 ? (int)atomicAdd(&u.gs->out_ctr, (uint32_t)cnt) : emitted;
-        s.bc[9] = 0;
+      int ob = emitted;
+      if (u.G > 1) {
+        if (threadIdx.x == 0) u.gs->cnt[u.rank] = (uint32_t)(lal + (take ? lel : 0));
+        if (!group_barrier(c, u, threadIdx.x == 0)) return false;
+        for (int i = threadIdx.x; i < kBins0; i += kThreads) u.gs->hlev[lev][i] = 0u;
+        ob += rank_prefix(c, u, u.gs->cnt);
       }
-      __syncthreads();
-      const int ob = s.bc[7];
-      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-        const float4 x = b4[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e < 0 || e >= u.n) continue;
-          if (coarse_digit(xs[j]) != (uint32_t)b0) continue;
-          const uint32_t key = f2key(xs[j]);
-          if ((key & pmask) != pval) continue;
-          const uint32_t d = (key >> shift) & dmask;
-          if (d > (uint32_t)bl || (take && d == (uint32_t)bl)) {
-            const int idx = atomicAdd(&s.bc[9], 1);
-            emit(c, u, ob + idx, u.s0 + e);
-          }
-        }
-      }
-      __syncthreads();
+      const uint32_t pm = pmask, pv = pval;
+      emit_ordered(c, u, ob, [&](int e, float x) {
+        (void)e;
+        if (coarse_digit(x) != (uint32_t)b0) return false;
+        const uint32_t key = f2key(x);
+        if ((key & pm) != pv) return false;
+        const uint32_t d = (key >> shift) & dmask;
+        return d > (uint32_t)bl || (take && d == (uint32_t)bl);
+      });
       emitted += abl + (take ? eql : 0);
       pmask |= dmask << shift;
       pval |= (uint32_t)bl << shift;
@@ -714,11 +794,10 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int above0, u
   if (u.G > 1) {
     if (threadIdx.x == 0) u.gs->tie_cnt[u.rank] = (uint32_t)local_tie;
     if (!group_barrier(c, u, threadIdx.x == 0)) return false;
-    int acc = 0;
-    for (int j = threadIdx.x; j < u.rank; j += kThreads) acc += (int)__ldcg(&u.gs->tie_cnt[j]);
-    prefix = block_sum(acc, s);
+    passed_barrier();
+    prefix = rank_prefix(c, u, u.gs->tie_cnt);
   }
-  const int tie_base = u.kr - need;  // every other entry fills [0, kr - need)
+  const int tie_base = emitted;  // every other entry fills [0, emitted)
   int running = prefix;
   for (int t0 = 0; t0 < u.n && running < need; t0 += 4 * kThreads) {
     int cnt = 0;
@@ -744,7 +823,7 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int above0, u
 
 // ------------------------------------------------------------- the unit
 
-__device__ void process_unit(Ctx& c, const UnitDesc& d) {
+__device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const SelectParams& P = c.p;
   Smem& s = c.s;
   Unit u;
@@ -767,8 +846,16 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d) {
   __syncthreads();  // the previous unit no longer uses shared memory
   TOPK_LOG(u.r, 1);
   // Issue the chunk's copies first: [s0, s0 + n) lies inside the row by construction
-  // of the plan, which the kernel validated against rows / max_len.
-  if (!copy_all && valid_plan_len && (u.G == 1 || u.gs != nullptr)) issue_chunk(c, u);
+  // of the plan, which the kernel validated against rows / max_len. The first static
+  // unit's copies were issued in the kernel prologue.
+  if (!copy_all && valid_plan_len && (u.G == 1 || u.gs != nullptr)) {
+    if (pre_issued) {
+      const char* src;
+      chunk_geometry(P, u, &src);
+    } else {
+      issue_chunk(c, u);
+    }
+  }
   for (int i = threadIdx.x; i < kBins0; i += kThreads) s.u.hist[i] = 0u;
   TOPK_MARK(g_select_trace, 1);
 
@@ -790,6 +877,15 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d) {
   u.t = P.row_to_table ? P.row_to_table[u.r] : u.r;
   u.kr = min(P.k, u.L);
   if (u.rank == 0) fill_row(c, u.r, u.kr, P.k);
+  if (!copy_all && u.n > 0 && threadIdx.x >= kThreads - 32) {
+    // Bring this chunk's page-table entries into L2 for the emission step.
+    const int32_t* t0 = P.table + (int64_t)u.t * P.table_ld + u.s0 / P.page_size;
+    const int32_t* t1 = P.table + (int64_t)u.t * P.table_ld + (u.s0 + u.n - 1) / P.page_size;
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(t0) & ~uintptr_t(127);
+    const uintptr_t l1 = reinterpret_cast<uintptr_t>(t1) & ~uintptr_t(127);
+    for (uintptr_t a = l0 + 128u * (threadIdx.x - (kThreads - 32)); a <= l1; a += 128u * 32u)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+  }
 
   // Short row: every position is selected, in position order.
   if (copy_all) {
@@ -804,6 +900,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d) {
   TOPK_LOG(u.r, 2);
 
   int b0, above0, eq0, la0, le0;
+  u.blocal = 0;
   if (!reduce_and_find(c, u, u.G > 1 ? u.gs->hist0 : nullptr, u.kr, u.n, true, b0, above0, eq0,
                        la0, le0))
     return;
@@ -814,119 +911,137 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d) {
   const bool compact = !all_eq && eq0 <= (u.G > 1 ? kGroupCap : kListCap);
   const bool fallback = !all_eq && !compact;
   const bool stage_cand = compact && le0 <= kListCap;  // else written straight to global
-
-  // Reserve output and candidate space for this CTA with one atomic (thread 0); its
-  // latency overlaps the classification pass, the result is read after it.
-  unsigned long long resv = 0ull;
-  if (u.G > 1 && threadIdx.x == 0) {
-    const unsigned long long cnt_out = (unsigned long long)(la0 + (all_eq ? le0 : 0));
-    const unsigned long long cnt_cand = compact ? (unsigned long long)le0 : 0ull;
-    resv = atomicAdd(reinterpret_cast<unsigned long long*>(&u.gs->out_ctr),
-                     cnt_out | (cnt_cand << 32));
-  }
-  if (threadIdx.x == 0) {
-    s.bc[9] = 0;   // staged emissions
-    s.bc[10] = 0;  // staged candidates
-  }
+  // Per-rank counts for the row's output offsets: staged emissions, candidates.
+  const int my_emit = la0 + (all_eq ? le0 : 0);
+  const int my_cand = compact ? le0 : 0;
+  if (u.G > 1 && threadIdx.x == 0) u.gs->cnt[u.rank] = (uint32_t)my_emit | ((uint32_t)my_cand << 16);
+  TOPK_MARK(g_select_trace, 16);
   __syncthreads();  // histogram region is free: reused for the staging lists
+  TOPK_MARK(g_select_trace, 17);
 
-  // Pass 2 over the resident chunk (warp-synchronous): stage positions above the
-  // threshold bin and boundary candidates, or fold the boundary keys (fallback).
+  // Pass 2 over the resident chunk: a float filter skips vectors below the threshold
+  // bin. First each
+  // thread counts the values it will stage (positions above the threshold bin,
+  // boundary candidates) or folds the boundary keys (fallback) and remembers up to
+  // two vectors that held any; a CTA scan turns the counts into offsets; then those
+  // threads write them (rescanning only when they saw more). No shared atomics; the
+  // staging order is deterministic. For a threshold bin on the positive side the
+  // bin's float bounds are exact, so values are classified by two compares.
   const float tlo = skip_below((uint32_t)b0);
+  const bool exact = b0 >= 2048 && b0 < 4095 && !fallback;
+  const float thi = exact ? skip_below((uint32_t)b0 + 1u) : 0.0f;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   uint32_t fa = 0xFFFFFFFFu, fo = 0u;
-  {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int vb = warp * 32; vb < u.nvec; vb += kThreads) {
-      const int v = vb + lane;
-      float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      if (v < u.nvec) x = b4[v];
-      const float m = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-      const bool hit = v < u.nvec && !(m < tlo);
-      if (!__any_sync(0xffffffffu, hit)) continue;
-      const float xs[4] = {x.x, x.y, x.z, x.w};
+  int na = 0, nc = 0;
+  int hv0 = -1, hv1 = -1, nhv = 0;
+  // classify one value: 0 below, 1 above (staged position), 2 boundary candidate
+  auto klass = [&](float x) -> int {
+    if (exact) return x >= tlo ? ((x >= thi || all_eq) ? 1 : 2) : 0;
+    const uint32_t dg = coarse_digit(x);
+    if (dg < (uint32_t)b0) return 0;
+    return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
+  };
+  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+    const float4 x = b4[v];
+    if (fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) < tlo) continue;
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    const int na0 = na, nc0 = nc;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = 4 * v - u.head + j;
-        const bool in = hit && e >= 0 && e < u.n;
-        const uint32_t dg = coarse_digit(xs[j]);
-        const bool above = in && (dg > (uint32_t)b0 || (all_eq && dg == (uint32_t)b0));
-        const bool cand = in && !all_eq && dg == (uint32_t)b0;
-        const int slot = warp_append(above, &s.bc[9]);
-        if (above && slot < TOPK_MAX_K) s.u.l.elist[slot] = u.s0 + e;
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e < 0 || e >= u.n) continue;
+      const int k = klass(xs[j]);
+      if (k == 1) {
+        ++na;
+      } else if (k == 2) {
         if (stage_cand) {
-          const int ci = warp_append(cand, &s.bc[10]);
-          if (cand && ci < kListCap) {
-            s.u.l.ckey[ci] = f2key(xs[j]);
-            s.u.l.cpos[ci] = (uint32_t)(u.s0 + e);
-          }
-        } else if (fallback && cand) {
+          ++nc;
+        } else if (fallback) {
           const uint32_t key = f2key(xs[j]);
           fa &= key;
           fo |= key;
         }
       }
     }
+    if (na + nc != na0 + nc0) {
+      if (nhv == 0) hv0 = v;
+      else if (nhv == 1) hv1 = v;
+      ++nhv;
+    }
   }
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 18] = global_timer_ns();
+  {
+    // slowest thread of the count pass
+    __shared__ unsigned long long tmax;
+    if (threadIdx.x == 0) tmax = 0;
+    __syncthreads();
+    atomicMax(&tmax, (unsigned long long)global_timer_ns());
+    __syncthreads();
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 20] = tmax;
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 21] = nhv;
+  }
+#endif
+  int tot_ac;
+  const int off_ac = block_excl_scan(na | (nc << 16), &tot_ac, s);
   if (threadIdx.x == 0) {
-    s.bc[7] = (int)(uint32_t)(resv & 0xFFFFFFFFull);
-    s.bc[8] = (int)(uint32_t)(resv >> 32);
+    s.bc[9] = tot_ac & 0xFFFF;  // staged emissions
+    s.bc[10] = tot_ac >> 16;    // staged candidates
   }
-  __syncthreads();
-  TOPK_MARK(g_select_trace, 4);
-  const int out_base = u.G > 1 ? s.bc[7] : 0;
-  const int cand_base = s.bc[8];
-  const int n_emit = min(s.bc[9], TOPK_MAX_K);
-
-  // Emit the staged positions (table lookups of the whole CTA in parallel).
-  for (int i = threadIdx.x; i < n_emit; i += kThreads) emit(c, u, out_base + i, s.u.l.elist[i]);
-
-  bool wrote_cand = false;  // this thread stored candidates that the last CTA reads
-  if (compact && u.G > 1) {
-    if (stage_cand) {
-      const int nc = min(s.bc[10], kListCap);
-      for (int i = threadIdx.x; i < nc; i += kThreads) {
-        if (cand_base + i < kGroupCap) {
-          u.gs->cand_key[cand_base + i] = s.u.l.ckey[i];
-          u.gs->cand_pos[cand_base + i] = s.u.l.cpos[i];
-          wrote_cand = true;
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 19] = global_timer_ns();
+#endif
+  if (na + nc > 0) {
+    int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
+    auto write = [&](int v) {
+      const float4 x = b4[v];
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = 4 * v - u.head + j;
+        if (e < 0 || e >= u.n) continue;
+        const int k = klass(xs[j]);
+        if (k == 1) {
+          if (oa < TOPK_MAX_K) s.u.l.elist[oa] = u.s0 + e;
+          ++oa;
+        } else if (k == 2 && stage_cand) {
+          if (oc < kListCap) {
+            s.u.l.ckey[oc] = f2key(xs[j]);
+            s.u.l.cpos[oc] = (uint32_t)(u.s0 + e);
+          }
+          ++oc;
         }
       }
+    };
+    if (nhv <= 2) {
+      write(hv0);
+      if (nhv == 2) write(hv1);
     } else {
-      // Too many local candidates to stage: a second pass writes them to global.
-      if (threadIdx.x == 0) s.bc[10] = 0;
-      __syncthreads();
       for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
         const float4 x = b4[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e < 0 || e >= u.n || coarse_digit(xs[j]) != (uint32_t)b0) continue;
-          const int gi = cand_base + atomicAdd(&s.bc[10], 1);
-          if (gi < kGroupCap) {
-            u.gs->cand_key[gi] = f2key(xs[j]);
-            u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
-            wrote_cand = true;
-          }
-        }
+        if (fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) < tlo) continue;
+        write(v);
       }
     }
   }
+  __syncthreads();  // staging lists and counts complete
+  TOPK_MARK(g_select_trace, 4);
+  if (fallback) block_and_or(fa, fo, s);
 
-  if (compact && u.G == 1) {
-    __syncthreads();
-    select_boundary(c, u, s.u.l.ckey, s.u.l.cpos, s.cst, min(eq0, kListCap), need, above0);
-  }
-
-  if (fallback) {
-    block_and_or(fa, fo, s);
-    if (u.G > 1) {
-      if (threadIdx.x == 0) {
-        atomicOr(&u.gs->and_key, ~fa);  // stored inverted so the reset value is 0
-        atomicOr(&u.gs->or_key, fo);
-      }
-      if (!group_barrier(c, u, threadIdx.x == 0)) return;
+  // Row-wide offsets (G > 1): one barrier publishes every rank's counts (and the
+  // fallback's key AND/OR); each CTA then clears the histogram bins it published.
+  int out_base = 0, cand_base = 0;
+  if (u.G > 1) {
+    if (fallback && threadIdx.x == 0) {
+      atomicOr(&u.gs->and_key, ~fa);  // stored inverted so the reset value is 0
+      atomicOr(&u.gs->or_key, fo);
+    }
+    if (!group_barrier(c, u, threadIdx.x == 0)) return;
+    for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
+    const int pre = rank_prefix(c, u, u.gs->cnt);
+    out_base = pre & 0xFFFF;
+    cand_base = pre >> 16;
+    if (fallback) {
       if (threadIdx.x == 0) {
         s.bc[11] = (int)~__ldcg(&u.gs->and_key);
         s.bc[12] = (int)__ldcg(&u.gs->or_key);
@@ -934,56 +1049,117 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d) {
       __syncthreads();
       fa = (uint32_t)s.bc[11];
       fo = (uint32_t)s.bc[12];
-      __syncthreads();
     }
-    if (!refine_in_place(c, u, b0, need, above0, fa, fo, le0)) return;
+  }
+  TOPK_MARK(g_select_trace, 5);
+
+  // Emit the staged positions (table lookups of the whole CTA in parallel).
+  const int n_emit = min(s.bc[9], TOPK_MAX_K);
+  for (int i = threadIdx.x; i < n_emit; i += kThreads) emit(c, u, out_base + i, s.u.l.elist[i]);
+
+  if (compact && u.G == 1) {
+    __syncthreads();
+    select_boundary(c, u, s.u.l.ckey, s.u.l.cpos, s.cst, min(eq0, kListCap), need, above0);
   }
 
-  if (u.G > 1) {
-    // End of the row for this CTA. The last one finishes the compact selection and
-    // clears the row's counters for the next call.
-    TOPK_MARK(g_select_trace, 5);
-    if (wrote_cand) __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t old = atomicAdd(&u.gs->fin, 1u);
-      s.bc[13] = (old + 1u == (uint32_t)u.G) ? 1 : 0;
-      __threadfence();
-    }
-    __syncthreads();
-    TOPK_MARK(g_select_trace, 6);
-    TOPK_LOG(u.r, s.bc[13] ? 7 : 6);
-    if (s.bc[13]) {
-      if (compact) {
-        uint32_t* lkey = reinterpret_cast<uint32_t*>(s.buf);
-        uint32_t* lpos = lkey + kGroupCap;
-        const int n = min(eq0, kGroupCap);
-        for (int i = threadIdx.x; i < n; i += kThreads) {
-          lkey[i] = __ldcg(&u.gs->cand_key[i]);
-          lpos[i] = __ldcg(&u.gs->cand_pos[i]);
+  if (compact && u.G > 1) {
+    // Publish this CTA's candidates at its offset, meet the row, then every CTA
+    // selects among all of them and emits its own selected candidates.
+    bool wrote = false;
+    if (stage_cand) {
+      const int nc = min(s.bc[10], kListCap);
+      for (int i = threadIdx.x; i < nc; i += kThreads) {
+        if (cand_base + i < kGroupCap) {
+          u.gs->cand_key[cand_base + i] = s.u.l.ckey[i];
+          u.gs->cand_pos[cand_base + i] = s.u.l.cpos[i];
+          wrote = true;
         }
-        __syncthreads();
-        select_boundary(c, u, lkey, lpos, s.cst, n, need, above0);
       }
-      TOPK_MARK(g_select_trace, 7);
-      const uint32_t levels = __ldcg(&u.gs->levels);
-      for (int i = threadIdx.x; i < kBins0; i += kThreads) {
-        u.gs->hist0[i] = 0u;
-        for (uint32_t l = 0; l < levels && l < 3; ++l) u.gs->hlev[l][i] = 0u;
+    } else {
+      const float4* b4c = reinterpret_cast<const float4*>(s.buf);
+      // ordered second pass straight to global (more local candidates than staging)
+      int cnt = 0;
+      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+        const float4 x = b4c[v];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 4 * v - u.head + j;
+          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) ++cnt;
+        }
       }
-      if (threadIdx.x == 0) {
-        u.gs->bar = 0u;
-        u.gs->fin = 0u;
-        u.gs->out_ctr = 0u;
-        u.gs->cand_ctr = 0u;
-        u.gs->and_key = 0u;
-        u.gs->or_key = 0u;
-        u.gs->levels = 0u;
+      int total;
+      int gi = cand_base + block_excl_scan(cnt, &total, s);
+      for (int v = threadIdx.x; v < u.nvec && cnt > 0; v += kThreads) {
+        const float4 x = b4c[v];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 4 * v - u.head + j;
+          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) {
+            if (gi < kGroupCap) {
+              u.gs->cand_key[gi] = f2key(xs[j]);
+              u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
+              wrote = true;
+            }
+            ++gi;
+          }
+        }
       }
-      TOPK_MARK(g_select_trace, 8);
     }
+    if (!group_barrier(c, u, wrote)) return;
+    TOPK_MARK(g_select_trace, 6);
+    const int n = min(eq0, kGroupCap);
+    uint32_t* lkey = reinterpret_cast<uint32_t*>(s.buf);
+    uint32_t* lpos = lkey + kGroupCap;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      lkey[i] = __ldcg(&u.gs->cand_key[i]);
+      lpos[i] = __ldcg(&u.gs->cand_pos[i]);
+    }
+    __syncthreads();
+    const int own0 = min(cand_base, n), own1 = min(cand_base + le0, n);
+    // The method must be the same in every CTA of the row (output index schemes
+    // differ), so it depends on the row-wide count only.
+    if (n <= kRankOwnMax) {
+      // rank this CTA's own candidates against all of them
+      for (int i = own0 + threadIdx.x; i < own1; i += kThreads) {
+        const uint32_t ki = lkey[i], pi = lpos[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+          const uint32_t kj = lkey[j], pj = lpos[j];
+          rank += (kj > ki || (kj == ki && pj < pi)) ? 1 : 0;
+        }
+        if (rank < need) emit(c, u, above0 + rank, (int)pi);
+      }
+    } else {
+      // radix-select among all candidates (same marks in every CTA), then each CTA
+      // emits its own marked candidates at their position among the marked ones
+      list_select(s, lkey, lpos, s.cst, n, need);
+      int cnt = 0, before = 0;
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        if (s.cst[i] == kSel) {
+          if (i < own0) ++before;
+        }
+      }
+      before = block_sum(before, s);
+      if (threadIdx.x == 0) s.bc[16] = 0;
+      __syncthreads();
+      for (int i0 = own0; i0 < own1; i0 += kThreads) {
+        const int i = i0 + threadIdx.x;
+        const bool sel = i < own1 && s.cst[i] == kSel;
+        int total;
+        const int off = block_excl_scan(sel ? 1 : 0, &total, s);
+        if (sel) emit(c, u, above0 + before + cnt + off, (int)lpos[i]);
+        cnt += total;
+      }
+    }
+    TOPK_MARK(g_select_trace, 7);
   }
+
+  if (fallback) {
+    if (!refine_in_place(c, u, b0, need, above0, fa, fo, le0)) return;
+  }
+  TOPK_MARK(g_select_trace, 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
@@ -1011,6 +1187,22 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     s.bc[28] = h2.w;  // dyn_period
     for (int i = 0; i < kPieces; ++i) mbar_init(&s.mbar[i], 1);
     fence_mbar_init();
+    // Start the first static unit's copies right away when the plan is valid.
+    const UnitDesc d = s.ud;
+    const bool ok = (uint32_t)h0.x == kMagic && h0.y == p.rows && h0.z == p.max_len &&
+                    h0.w == (int)gridDim.x && h2.y == 0 && h1.y > 0;
+    s.bc[19] = 0;
+    if (ok && d.row >= 0 && d.len >= 0 && d.len <= p.max_len && d.len > p.k &&
+        (d.G == 1 || d.group >= 0)) {
+      Unit u;
+      u.r = d.row;
+      u.s0 = d.s0;
+      u.n = d.n;
+      const char* src;
+      const uint32_t bytes = chunk_geometry(p, u, &src);
+      issue_copies(s, src, bytes, u.npieces);
+      s.bc[19] = 1;
+    }
   }
   __syncthreads();
   const bool bad = (uint32_t)s.bc[20] != kMagic || s.bc[21] != p.rows || s.bc[22] != p.max_len ||
@@ -1032,6 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   TOPK_LOG(-1, 0);
 #endif
 
+  const bool pre_issued = s.bc[19] != 0;
   Ctx c{p, h, s, 0u};
   for (int w = 0; w < waves; ++w) {
     UnitDesc d;
@@ -1044,7 +1237,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
       d = s.ud;
     }
     TOPK_LOG(d.row, 15);
-    if (d.row >= 0) process_unit(c, d);
+    if (d.row >= 0) process_unit(c, d, w == 0 && pre_issued);
   }
 
   const int2* singles = reinterpret_cast<const int2*>(p.ws + lay.singles);
@@ -1073,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     d.G = 1;
     d.group = -1;
     d.pad = 0;
-    process_unit(c, d);
+    process_unit(c, d, false);
   }
   TOPK_MARK(g_select_trace, 9);
 }
@@ -1087,7 +1280,7 @@ extern "C" int topk_trace_log(uint64_t* host, int* counts) {
   return cudaMemcpyFromSymbol(counts, g_select_log_n, sizeof(int) * kMaxGrid) == cudaSuccess ? 0 : -9;
 }
 extern "C" int topk_trace_select(uint64_t* host, int n) {
-  if (n > kMaxGrid * 16) n = kMaxGrid * 16;
+  if (n > kMaxGrid * 32) n = kMaxGrid * 32;
   return cudaMemcpyFromSymbol(host, g_select_trace, sizeof(uint64_t) * n) == cudaSuccess ? 0 : -9;
 }
 #endif
