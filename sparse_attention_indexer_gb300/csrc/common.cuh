@@ -27,7 +27,7 @@ constexpr int kLevelBits = 12;             // in-place refinement digit width
 constexpr int kListCap = 1024;             // single-CTA compact candidate list (smem)
 constexpr int kRankMax = 192;              // boundary sets up to this size: rank counting
 constexpr int kRankOwnMax = 1024;          // multi-CTA rows: each CTA ranks its own candidates
-constexpr int kGroupCap = 4096;            // multi-CTA compact candidate list (global)
+constexpr int kGroupCap = 8192;            // multi-CTA compact candidate list (global)
 constexpr int kListBins = 256;             // digit width 8 for list refinement
 constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
 constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // bounded waits: 200 ms
@@ -73,18 +73,17 @@ struct __align__(16) UnitDesc {
   int32_t rank, G, group, pad;
 };
 
-// Per multi-CTA row. `bar` is a generation barrier counter: every CTA of the row
-// adds 1 per barrier, so it stays a multiple of G between barriers and is never
-// reset by the select kernel. The histograms are cleared by the CTAs that wrote
-// them once a later barrier shows every CTA has read them; the per-rank arrays are
-// overwritten by every call.
+// Per multi-CTA row. Row barriers use one flag word per rank: (barriers passed by
+// that rank) << 32 | a 32-bit payload, written with release semantics; a waiter
+// acquires every rank's flag, so a barrier also delivers each rank's payload (its
+// counts). Flags only grow and are never reset by the select kernel. The histograms
+// are cleared by the CTAs that wrote them once a later barrier shows every CTA has
+// read them; the candidate slots are overwritten by every call.
 struct GroupState {
-  unsigned long long bar;  // barrier arrivals (generation = bar / G)
-  uint32_t and_key;        // ~AND of boundary keys (stored inverted: reset value 0)
-  uint32_t or_key;         // OR of boundary keys
-  uint32_t pad[60];
-  uint32_t cnt[kMaxGrid];      // per rank: staged emissions | candidates << 16
-  uint32_t tie_cnt[kMaxGrid];  // per rank: tied values (in-place refinement)
+  unsigned long long flag[kMaxGrid];
+  uint32_t and_key;  // ~AND of boundary keys (stored inverted: reset value 0)
+  uint32_t or_key;   // OR of boundary keys
+  uint32_t pad[62];
   uint32_t hist0[kBins0];
   uint32_t hlev[3][1 << kLevelBits];
   uint32_t cand_key[kGroupCap];
@@ -214,6 +213,10 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {

@@ -65,6 +65,7 @@ struct __align__(16) Smem {
     } l;
   } u;
   uint8_t cst[kGroupCap];         // list-selection state
+  uint32_t pay[kMaxGrid];         // per-rank payloads delivered by the last row barrier
   uint32_t hist8[kListBins];
   uint64_t mbar[kPieces];
   int wsum[kWarps];
@@ -208,7 +209,8 @@ struct Unit {
   int r, rank, G, L, kr, t, s0, n, head, nvec, npieces;
   int blocal;  // lowest coarse bin this CTA published to the row histogram
   GroupState* gs;
-  uint32_t bar_seq;  // barriers passed in this unit
+  uint32_t bar_seq;    // barriers passed in this unit
+  uint32_t flag_base;  // barriers this rank had passed before this unit
 };
 
 struct Ctx {
@@ -250,52 +252,58 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
   }
 }
 
-// Group barrier among the G CTAs of a row. All threads call it; a thread that wrote
-// row state to global memory (histogram reductions, counts, candidates) passes
-// wrote = true and fences its own writes first, so that they are performed before
-// thread 0 arrives (an arrival by one thread does not order other warps' writes
-// still in flight). Generation barrier: the arrival returns the count before it,
-// and the barrier opens when the count reaches the next multiple of G, so the
-// counter never needs a reset. The waiting side acquires. Returns false if the
-// bounded wait expired (status set).
-__device__ bool group_barrier(Ctx& c, Unit& u, bool wrote) {
+// Row barrier among the G CTAs of a row. All threads call it; a thread that wrote
+// row state to global memory (histogram reductions, candidates) passes wrote = true
+// and fences its own writes first, so that they are performed before thread 0
+// arrives (an arrival by one thread does not order other warps' writes still in
+// flight). Thread 0 arrives by a release store of its rank's flag, (barriers passed)
+// << 32 | payload; the lanes of warp 0 acquire every rank's flag. Afterwards s.pay[j]
+// holds rank j's payload and *prefix (if non-null) the sum of the payloads of ranks
+// below this one. Returns false if a bounded wait expired (status set).
+__device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
   if (wrote) __threadfence();
   __syncthreads();
   u.bar_seq += 1;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned long long G = (unsigned long long)u.G;
-    const unsigned long long old = atomicAdd(&u.gs->bar, 1ull);
-    const unsigned long long target = (old / G + 1ull) * G;
-    bool ok = old + 1ull == target || ld_acquire_u64(&u.gs->bar) >= target;
-    if (!ok) {
-      const uint64_t t0 = global_timer_ns();
-      while (true) {
-        if (ld_acquire_u64(&u.gs->bar) >= target) {
-          ok = true;
-          break;
-        }
-        if (global_timer_ns() - t0 > kWaitNs) break;
-      }
+  const uint32_t my = u.flag_base + u.bar_seq;
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
     }
-    __threadfence();
-    c.s.bc[15] = ok ? 1 : 0;
+    __syncwarp();
+    int acc = 0;
+    bool ok = true;
+    int stuck = -1;
+    for (int j = threadIdx.x; j < u.G && ok; j += 32) {
+      unsigned long long v = ld_acquire_u64(&u.gs->flag[j]);
+      if ((uint32_t)(v >> 32) < my) {
+        const uint64_t t0 = global_timer_ns();
+        while ((uint32_t)((v = ld_acquire_u64(&u.gs->flag[j])) >> 32) < my) {
+          if (global_timer_ns() - t0 > kWaitNs) {
+            ok = false;
+            stuck = j;
+            break;
+          }
+        }
+      }
+      c.s.pay[j] = (uint32_t)v;
+      if (j < u.rank) acc += (int)(uint32_t)v;
+    }
+    const bool all_ok = __all_sync(0xffffffffu, ok);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (!ok) {
       set_status(c.h, TOPK_STATUS_TIMEOUT);
-      record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, (int)(ld_acquire_u64(&u.gs->bar) % G),
-                     (int)G);
+      record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, stuck, (int)my);
+    }
+    if (threadIdx.x == 0) {
+      c.s.bc[15] = all_ok ? 1 : 0;
+      c.s.bc[17] = acc;
     }
   }
   __syncthreads();
+  if (prefix) *prefix = c.s.bc[17];
   return c.s.bc[15] != 0;
-}
-
-// Exclusive prefix over ranks < u.rank of the per-rank words gs->cnt (two 16-bit
-// fields), published before the last barrier.
-__device__ int rank_prefix(Ctx& c, const Unit& u, const uint32_t* arr) {
-  int acc = 0;
-  for (int j = threadIdx.x; j < u.rank; j += kThreads) acc += (int)__ldcg(&arr[j]);
-  return block_sum(acc, c.s);
 }
 
 __device__ __forceinline__ unsigned long long warp_incl_scan64(unsigned long long x) {
@@ -398,7 +406,7 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
         red_add_u32(&ghist[b0 + j], loc[j]);
         wrote = true;
       }
-    if (!group_barrier(c, u, wrote)) return false;
+    if (!group_sync(c, u, wrote, 0u, nullptr)) return false;
     if (b0 + 7 >= blocal) {
       load8_cg(&ghist[b0], glob);
     } else {
@@ -760,10 +768,10 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, 
       const bool take = (eql == need);
       int ob = emitted;
       if (u.G > 1) {
-        if (threadIdx.x == 0) u.gs->cnt[u.rank] = (uint32_t)(lal + (take ? lel : 0));
-        if (!group_barrier(c, u, threadIdx.x == 0)) return false;
+        int pre;
+        if (!group_sync(c, u, false, (uint32_t)(lal + (take ? lel : 0)), &pre)) return false;
         for (int i = threadIdx.x; i < kBins0; i += kThreads) u.gs->hlev[lev][i] = 0u;
-        ob += rank_prefix(c, u, u.gs->cnt);
+        ob += pre;
       }
       const uint32_t pm = pmask, pv = pval;
       emit_ordered(c, u, ob, [&](int e, float x) {
@@ -792,10 +800,8 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, 
   const uint32_t T = pval;
   int prefix = 0;
   if (u.G > 1) {
-    if (threadIdx.x == 0) u.gs->tie_cnt[u.rank] = (uint32_t)local_tie;
-    if (!group_barrier(c, u, threadIdx.x == 0)) return false;
+    if (!group_sync(c, u, false, (uint32_t)local_tie, &prefix)) return false;
     passed_barrier();
-    prefix = rank_prefix(c, u, u.gs->tie_cnt);
   }
   const int tie_base = emitted;  // every other entry fills [0, emitted)
   int running = prefix;
@@ -876,6 +882,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   }
   u.t = P.row_to_table ? P.row_to_table[u.r] : u.r;
   u.kr = min(P.k, u.L);
+  u.flag_base = u.G > 1 ? (uint32_t)(__ldcg(&u.gs->flag[u.rank]) >> 32) : 0u;
   if (u.rank == 0) fill_row(c, u.r, u.kr, P.k);
   if (!copy_all && u.n > 0 && threadIdx.x >= kThreads - 32) {
     // Bring this chunk's page-table entries into L2 for the emission step.
@@ -914,7 +921,6 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   // Per-rank counts for the row's output offsets: staged emissions, candidates.
   const int my_emit = la0 + (all_eq ? le0 : 0);
   const int my_cand = compact ? le0 : 0;
-  if (u.G > 1 && threadIdx.x == 0) u.gs->cnt[u.rank] = (uint32_t)my_emit | ((uint32_t)my_cand << 16);
   TOPK_MARK(g_select_trace, 16);
   __syncthreads();  // histogram region is free: reused for the staging lists
   TOPK_MARK(g_select_trace, 17);
@@ -933,7 +939,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   uint32_t fa = 0xFFFFFFFFu, fo = 0u;
   int na = 0, nc = 0;
-  int hv0 = -1, hv1 = -1, nhv = 0;
+  int hv0 = -1, hv1 = -1, hv2 = -1, hv3 = -1, nhv = 0;
   // classify one value: 0 below, 1 above (staged position), 2 boundary candidate
   auto klass = [&](float x) -> int {
     if (exact) return x >= tlo ? ((x >= thi || all_eq) ? 1 : 2) : 0;
@@ -941,32 +947,62 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     if (dg < (uint32_t)b0) return 0;
     return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
   };
-  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-    const float4 x = b4[v];
-    if (fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) < tlo) continue;
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    const int na0 = na, nc0 = nc;
+  auto count = [&](int v, const float4& x) {
+    const int e0 = 4 * v - u.head;
+    int a = 0, cd = 0;
+    if (exact && e0 >= 0 && e0 + 3 < u.n) {
+      // full vector, exact bin bounds: branch-free
+      const int ge = (x.x >= tlo) + (x.y >= tlo) + (x.z >= tlo) + (x.w >= tlo);
+      a = all_eq ? ge : (x.x >= thi) + (x.y >= thi) + (x.z >= thi) + (x.w >= thi);
+      cd = ge - a;
+    } else {
+      const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * v - u.head + j;
-      if (e < 0 || e >= u.n) continue;
-      const int k = klass(xs[j]);
-      if (k == 1) {
-        ++na;
-      } else if (k == 2) {
-        if (stage_cand) {
-          ++nc;
-        } else if (fallback) {
-          const uint32_t key = f2key(xs[j]);
-          fa &= key;
-          fo |= key;
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + j;
+        if (e < 0 || e >= u.n) continue;
+        const int k = klass(xs[j]);
+        if (k == 1) {
+          ++a;
+        } else if (k == 2) {
+          ++cd;
+          if (fallback) {
+            const uint32_t key = f2key(xs[j]);
+            fa &= key;
+            fo |= key;
+          }
         }
       }
     }
-    if (na + nc != na0 + nc0) {
+    if (!stage_cand) cd = 0;
+    if (a + cd) {
+      na += a;
+      nc += cd;
       if (nhv == 0) hv0 = v;
       else if (nhv == 1) hv1 = v;
+      else if (nhv == 2) hv2 = v;
+      else if (nhv == 3) hv3 = v;
       ++nhv;
+    }
+  };
+  {
+    auto vmax = [](const float4& x) { return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)); };
+    int v = threadIdx.x;
+    for (; v + 3 * kThreads < u.nvec; v += 4 * kThreads) {
+      const float4 x0 = b4[v], x1 = b4[v + kThreads];
+      const float4 x2 = b4[v + 2 * kThreads], x3 = b4[v + 3 * kThreads];
+      const bool h0 = !(vmax(x0) < tlo), h1 = !(vmax(x1) < tlo);
+      const bool h2 = !(vmax(x2) < tlo), h3 = !(vmax(x3) < tlo);
+      if (h0 | h1 | h2 | h3) {
+        if (h0) count(v, x0);
+        if (h1) count(v + kThreads, x1);
+        if (h2) count(v + 2 * kThreads, x2);
+        if (h3) count(v + 3 * kThreads, x3);
+      }
+    }
+    for (; v < u.nvec; v += kThreads) {
+      const float4 x0 = b4[v];
+      if (!(vmax(x0) < tlo)) count(v, x0);
     }
   }
 #ifdef TOPK_TRACE
@@ -1013,9 +1049,11 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         }
       }
     };
-    if (nhv <= 2) {
+    if (nhv <= 4) {
       write(hv0);
-      if (nhv == 2) write(hv1);
+      if (nhv >= 2) write(hv1);
+      if (nhv >= 3) write(hv2);
+      if (nhv >= 4) write(hv3);
     } else {
       for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
         const float4 x = b4[v];
@@ -1024,11 +1062,71 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       }
     }
   }
+#ifdef TOPK_TRACE
+  {
+    __shared__ unsigned long long wmax;
+    if (threadIdx.x == 0) wmax = 0;
+    const unsigned long long tnow = global_timer_ns();
+    __syncthreads();
+    atomicMax(&wmax, tnow);
+    __syncthreads();
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 22] = wmax;
+  }
+#endif
   __syncthreads();  // staging lists and counts complete
   TOPK_MARK(g_select_trace, 4);
   if (fallback) block_and_or(fa, fo, s);
 
-  // Row-wide offsets (G > 1): one barrier publishes every rank's counts (and the
+  // Multi-CTA rows: per-rank candidate slots let one barrier carry both the counts
+  // (in the flags) and the candidates when the row's boundary bin is small enough
+  // for every rank to fit its slot; otherwise candidates wait for the offsets.
+  const int slot_cap = u.G > 1 ? kGroupCap / u.G : 0;
+  const bool slots = compact && u.G > 1 && eq0 <= slot_cap;
+  bool wrote_cand = false;
+  auto write_candidates = [&](int base) {
+    // staged list, or an ordered second pass straight to global
+    if (stage_cand) {
+      const int nc = min(s.bc[10], kListCap);
+      for (int i = threadIdx.x; i < nc; i += kThreads)
+        if (base + i < kGroupCap) {
+          u.gs->cand_key[base + i] = s.u.l.ckey[i];
+          u.gs->cand_pos[base + i] = s.u.l.cpos[i];
+          wrote_cand = true;
+        }
+    } else {
+      int cnt = 0;
+      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+        const float4 x = b4[v];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 4 * v - u.head + j;
+          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) ++cnt;
+        }
+      }
+      int total;
+      int gi = base + block_excl_scan(cnt, &total, s);
+      for (int v = threadIdx.x; v < u.nvec && cnt > 0; v += kThreads) {
+        const float4 x = b4[v];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = 4 * v - u.head + j;
+          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) {
+            if (gi < kGroupCap) {
+              u.gs->cand_key[gi] = f2key(xs[j]);
+              u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
+              wrote_cand = true;
+            }
+            ++gi;
+          }
+        }
+      }
+    }
+  };
+  if (slots) write_candidates(u.rank * slot_cap);
+
+  // Row-wide offsets (G > 1): one barrier delivers every rank's counts (and the
   // fallback's key AND/OR); each CTA then clears the histogram bins it published.
   int out_base = 0, cand_base = 0;
   if (u.G > 1) {
@@ -1036,9 +1134,11 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       atomicOr(&u.gs->and_key, ~fa);  // stored inverted so the reset value is 0
       atomicOr(&u.gs->or_key, fo);
     }
-    if (!group_barrier(c, u, threadIdx.x == 0)) return;
+    int pre;
+    if (!group_sync(c, u, wrote_cand || (fallback && threadIdx.x == 0),
+                    (uint32_t)my_emit | ((uint32_t)my_cand << 16), &pre))
+      return;
     for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
-    const int pre = rank_prefix(c, u, u.gs->cnt);
     out_base = pre & 0xFFFF;
     cand_base = pre >> 16;
     if (fallback) {
@@ -1063,60 +1163,47 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   }
 
   if (compact && u.G > 1) {
-    // Publish this CTA's candidates at its offset, meet the row, then every CTA
-    // selects among all of them and emits its own selected candidates.
-    bool wrote = false;
-    if (stage_cand) {
-      const int nc = min(s.bc[10], kListCap);
-      for (int i = threadIdx.x; i < nc; i += kThreads) {
-        if (cand_base + i < kGroupCap) {
-          u.gs->cand_key[cand_base + i] = s.u.l.ckey[i];
-          u.gs->cand_pos[cand_base + i] = s.u.l.cpos[i];
-          wrote = true;
-        }
-      }
-    } else {
-      const float4* b4c = reinterpret_cast<const float4*>(s.buf);
-      // ordered second pass straight to global (more local candidates than staging)
-      int cnt = 0;
-      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-        const float4 x = b4c[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) ++cnt;
-        }
-      }
-      int total;
-      int gi = cand_base + block_excl_scan(cnt, &total, s);
-      for (int v = threadIdx.x; v < u.nvec && cnt > 0; v += kThreads) {
-        const float4 x = b4c[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) {
-            if (gi < kGroupCap) {
-              u.gs->cand_key[gi] = f2key(xs[j]);
-              u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
-              wrote = true;
-            }
-            ++gi;
-          }
-        }
-      }
-    }
-    if (!group_barrier(c, u, wrote)) return;
-    TOPK_MARK(g_select_trace, 6);
+    // Every CTA gathers all candidates (in rank order) and selects among them;
+    // each emits its own selected candidates.
     const int n = min(eq0, kGroupCap);
     uint32_t* lkey = reinterpret_cast<uint32_t*>(s.buf);
     uint32_t* lpos = lkey + kGroupCap;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      lkey[i] = __ldcg(&u.gs->cand_key[i]);
-      lpos[i] = __ldcg(&u.gs->cand_pos[i]);
+    __syncthreads();  // staged candidates (in the histogram region) no longer needed
+    if (slots) {
+      // s.pay[j] := exclusive prefix of the ranks' candidate counts (warp 0), then
+      // every thread fetches its share of candidates with independent loads.
+      if (threadIdx.x < 32) {
+        int carry = 0;
+        for (int j0 = 0; j0 < u.G; j0 += 32) {
+          const int j = j0 + threadIdx.x;
+          const int lj = j < u.G ? (int)(s.pay[j] >> 16) : 0;
+          const int incl = warp_incl_scan(lj);
+          if (j < u.G) s.pay[j] = (uint32_t)(carry + incl - lj);
+          carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        int lo = 0, hi = u.G - 1;  // last rank whose prefix <= i
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if ((int)s.pay[mid] <= i) lo = mid;
+          else hi = mid - 1;
+        }
+        const int src = lo * slot_cap + (i - (int)s.pay[lo]);
+        lkey[i] = __ldcg(&u.gs->cand_key[src]);
+        lpos[i] = __ldcg(&u.gs->cand_pos[src]);
+      }
+    } else {
+      write_candidates(cand_base);
+      if (!group_sync(c, u, wrote_cand, 0u, nullptr)) return;
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        lkey[i] = __ldcg(&u.gs->cand_key[i]);
+        lpos[i] = __ldcg(&u.gs->cand_pos[i]);
+      }
     }
     __syncthreads();
+    TOPK_MARK(g_select_trace, 6);
     const int own0 = min(cand_base, n), own1 = min(cand_base + le0, n);
     // The method must be the same in every CTA of the row (output index schemes
     // differ), so it depends on the row-wide count only.
@@ -1136,14 +1223,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       // emits its own marked candidates at their position among the marked ones
       list_select(s, lkey, lpos, s.cst, n, need);
       int cnt = 0, before = 0;
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        if (s.cst[i] == kSel) {
-          if (i < own0) ++before;
-        }
-      }
+      for (int i = threadIdx.x; i < own0; i += kThreads)
+        if (s.cst[i] == kSel) ++before;
       before = block_sum(before, s);
-      if (threadIdx.x == 0) s.bc[16] = 0;
-      __syncthreads();
       for (int i0 = own0; i0 < own1; i0 += kThreads) {
         const int i = i0 + threadIdx.x;
         const bool sel = i < own1 && s.cst[i] == kSel;
