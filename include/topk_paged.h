@@ -57,7 +57,8 @@ enum {
   TOPK_ERR_ALIGN = -8,       /* scores not 4-byte aligned / outputs not 4-byte aligned */
   TOPK_ERR_CUDA = -9,        /* a CUDA runtime call failed (launch, attribute query) */
   TOPK_ERR_DEVICE = -10,     /* current device cannot run the kernels (not sm_103) */
-  TOPK_ERR_CHUNK = -11       /* forced chunk size outside [16, topk_chunk_capacity()] */
+  TOPK_ERR_CHUNK = -11,      /* forced chunk size outside [16, topk_chunk_capacity()] */
+  TOPK_ERR_STATIC_ROWS = -12 /* rows above TOPK_STATIC_MAX_ROWS (topk_select_paged_noalloc) */
 };
 
 /* Device status bits (sticky, OR-ed together; 0 = no error). */
@@ -132,6 +133,37 @@ const char* topk_status_str(int code);
 
 /* Number of CTAs of the persistent select grid on the current device. */
 int topk_grid_size(void);
+
+/* Limits of topk_select_paged_noalloc: its scratch is a fixed 10 MiB array in the
+ * library's device image, enough for the plan and group states of 64 rows. */
+#define TOPK_STATIC_MAX_ROWS 64
+#define TOPK_STATIC_SCRATCH_BYTES (10u * 1024u * 1024u)
+
+/* Plan + select + page translation in one call that allocates nothing and takes no
+ * workspace. The pages have no counterpart of this entry point: it serves callers
+ * that cannot provide device memory (a plain C host without a device allocator, a
+ * plug-in in an engine whose free device memory is all reserved for the KV cache,
+ * code that must not call cudaMalloc/cudaFree because they synchronize the device).
+ * It enqueues topk_plan and then topk_select_paged on `stream`, both on a scratch
+ * array of TOPK_STATIC_SCRATCH_BYTES bytes that is a file-scope __device__ object of
+ * the library (allocated when the module loads). The planning kernel clears what
+ * must start at zero (group-state flags, histograms, counters, the status word) on
+ * every call, so every call starts clean.
+ *   arguments   as for topk_select_paged (scores, ld, lens, rows, max_len, k,
+ *               block_table, table_ld, row_to_table, page_size, out_slots, out_pos)
+ *   status      device int32 [1] or NULL: receives this call's device status bits
+ *               (TOPK_STATUS_*) once the stream reaches the end of the call
+ * Returns TOPK_ERR_STATIC_ROWS for rows > TOPK_STATIC_MAX_ROWS, otherwise the codes
+ * of topk_plan / topk_select_paged; any negative return enqueued nothing.
+ * The first call on each device looks up the scratch array's address with
+ * cudaGetSymbolAddress (with that device current) and queries the device; make that
+ * first call before any stream capture begins. There is one scratch array per
+ * device: calls that overlap in time on one device (two streams, two host threads)
+ * race on it and give undefined results; serialize them on one stream. */
+int topk_select_paged_noalloc(const float* scores, int64_t ld, const int32_t* lens, int rows,
+                              int max_len, int k, const int32_t* block_table, int64_t table_ld,
+                              const int32_t* row_to_table, int page_size, int32_t* out_slots,
+                              int32_t* out_pos, int32_t* status, topk_stream_t stream);
 
 #ifdef __cplusplus
 }

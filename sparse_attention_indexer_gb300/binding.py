@@ -24,11 +24,14 @@ STATUS_TABLE_ENTRY = 4
 STATUS_SLOT_OVERFLOW = 8
 STATUS_TIMEOUT = 16
 STATUS_PLAN_MISMATCH = 32
+ERR_STATIC_ROWS = -12
+STATIC_MAX_ROWS = 64
 
 EXPORTS = (
     "topk_workspace_bytes", "topk_max_row_len", "topk_chunk_capacity", "topk_plan",
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
+    "topk_select_paged_noalloc",
 )
 
 
@@ -56,6 +59,8 @@ _SIGS = {
     "topk_status_str": (_c.c_char_p, [_c.c_int]),
     "topk_plan_host": (_c.c_int, [_VP, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_size_t]),
     "topk_layout_info": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int64), _c.c_int]),
+    "topk_select_paged_noalloc": (_c.c_int, [_VP, _c.c_int64, _VP, _c.c_int, _c.c_int, _c.c_int,
+                                             _VP, _c.c_int64, _VP, _c.c_int, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -141,6 +146,16 @@ def topk_select_paged(scores, ld: int, lens, rows: int, max_len: int, k: int, bl
         _ptr(scores), int(ld), _ptr(lens), int(rows), int(max_len), int(k), _ptr(block_table),
         int(table_ld), _ptr(row_to_table), int(page_size), _ptr(out_slots), _ptr(out_pos),
         _ptr(workspace), _stream(stream)), "topk_select_paged")
+
+
+def topk_select_paged_noalloc(scores, ld: int, lens, rows: int, max_len: int, k: int,
+                              block_table, table_ld: int, row_to_table, page_size: int,
+                              out_slots, out_pos, status, stream=None) -> int:
+    """No workspace argument: the library's static device scratch serves the call."""
+    return _check(lib().topk_select_paged_noalloc(
+        _ptr(scores), int(ld), _ptr(lens), int(rows), int(max_len), int(k), _ptr(block_table),
+        int(table_ld), _ptr(row_to_table), int(page_size), _ptr(out_slots), _ptr(out_pos),
+        _ptr(status), _stream(stream)), "topk_select_paged_noalloc")
 
 
 def topk_read_status(workspace, stream=None) -> int:

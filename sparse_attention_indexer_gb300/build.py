@@ -1,6 +1,6 @@
 """Builds the CUDA library libtopk_paged.so in-tree for sm_103a with nvcc.
 
-Three translation units are compiled in parallel and linked into one shared library
+Four translation units are compiled in parallel and linked into one shared library
 that exports the C ABI of include/topk_paged.h (no torch types cross it).
 """
 from __future__ import annotations
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
-SOURCES = ["select.cu", "plan.cu", "abi.cu"]
+SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -176,6 +176,7 @@ const char* topk_status_str(int code) {
     case TOPK_ERR_CUDA: return "a CUDA runtime call failed";
     case TOPK_ERR_DEVICE: return "the current device cannot run the kernels (needs sm_103)";
     case TOPK_ERR_CHUNK: return "forced chunk outside [16, chunk capacity]";
+    case TOPK_ERR_STATIC_ROWS: return "rows above TOPK_STATIC_MAX_ROWS (64) for the no-allocation entry point";
     default: break;
   }
   if (code > 0) {

@@ -1,0 +1,85 @@
+"""The no-allocation entry point (topk_select_paged_noalloc) against the workspace
+entry points (topk_plan + topk_select_paged), through the C ABI.
+
+Collected last on purpose: it must pass both alone in a fresh process and after every
+other GPU test has used the library.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from sparse_attention_indexer_gb300 import binding as B  # noqa: E402
+from tests._gpu import compare_with_oracle, run_gpu, to_dev  # noqa: E402
+
+
+def _by_position(pos, slots):
+    """Rows as sets: each row's (position, slot) pairs ordered by position."""
+    order = np.argsort(pos, axis=1, kind="stable")
+    return np.take_along_axis(pos, order, 1), np.take_along_axis(slots, order, 1)
+
+
+class _Call:
+    """Device inputs and outputs of one no-allocation call, all made up front."""
+
+    def __init__(self, b, k):
+        self.b, self.k = b, k
+        self.scores, self.lens, self.table, self.r2t = to_dev(b)
+        self.slots = torch.full((b.rows, k), -5, dtype=torch.int32, device="cuda")
+        self.pos = torch.full((b.rows, k), -5, dtype=torch.int32, device="cuda")
+        self.status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+
+    def run(self):
+        b = self.b
+        return B.topk_select_paged_noalloc(
+            self.scores, b.ld, self.lens, b.rows, b.max_len, self.k, self.table,
+            b.block_table.shape[1], self.r2t, b.page_size, self.slots, self.pos, self.status)
+
+    def result(self):
+        return self.slots.cpu().numpy(), self.pos.cpu().numpy(), int(self.status.item())
+
+
+def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
+    a = W.verify_80k()                       # 7 rows of 80K: multi-CTA rows
+    c = W.adversarial(rows=B.STATIC_MAX_ROWS, max_len=32768)  # at the row limit
+    calls = [_Call(a, a.k), _Call(c, 512), _Call(a, 100)]
+    calls[0].run()  # first call per device does the set-up; results checked below
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    reserved0 = torch.cuda.memory_reserved()
+    for call in calls:
+        call.slots.fill_(-5)
+        call.pos.fill_(-5)
+    for call in calls:  # back to back on one stream, no sync in between
+        assert call.run() == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.memory_reserved() == reserved0
+    for i, call in enumerate(calls):
+        s, p, st = call.result()
+        assert st == 0, B.status_str(st)
+        ref_s, ref_p, ref_st = run_gpu(call.b, k=call.k)
+        assert ref_st == 0
+        gp, gs = _by_position(p, s)
+        rp, rs = _by_position(ref_p, ref_s)
+        assert np.array_equal(gp, rp), f"call {i}: positions differ from the workspace path"
+        assert np.array_equal(gs, rs), f"call {i}: slots differ from the workspace path"
+    s, p, _ = calls[0].result()
+    compare_with_oracle(a, a.k, s, p)
+
+
+def test_noalloc_rejects_rows_above_limit():
+    b = W.adversarial(rows=B.STATIC_MAX_ROWS + 1, max_len=2048)
+    call = _Call(b, 16)
+    with pytest.raises(B.TopKError) as ei:
+        call.run()
+    assert ei.value.code == B.ERR_STATIC_ROWS
+    torch.cuda.synchronize()
+    assert torch.all(call.slots == -5) and torch.all(call.status == -1)  # nothing enqueued
+    assert "TOPK_STATIC_MAX_ROWS" in B.status_str(B.ERR_STATIC_ROWS)
