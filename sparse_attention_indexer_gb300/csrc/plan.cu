@@ -12,6 +12,9 @@
 // takes without claiming a ticket.
 #include <cuda_runtime.h>
 
+#include <climits>
+#include <cstddef>
+
 #include "common.cuh"
 #include "plan_logic.cuh"
 
@@ -25,7 +28,9 @@ __device__ uint64_t g_plan_trace[kMaxGrid * 32];
 
 constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
-constexpr int kLensCache = 4096;  // batches up to this many rows plan from shared memory
+constexpr int kLensCache = 4096;     // batches up to this many rows plan from shared memory
+constexpr int kCandidateRows = 64;   // chunk search by parallel candidates up to this many rows
+constexpr int kZeroPerThread = 4;    // 16-byte stores per thread of a zeroing block
 
 struct PlanSmem {
   long long red64[kPlanWarps];
@@ -35,12 +40,29 @@ struct PlanSmem {
   int32_t multi_g[kMaxGroups];
   int32_t multi_wave[kMaxGroups];
   int32_t multi_cta[kMaxGroups];
-  uint32_t busy[kMaxGrid / 32];  // CTAs with static units
+  uint8_t busy[kMaxGrid];  // CTAs with static units
   unsigned bucket_mask;
   int32_t lens[kLensCache];
 };
 
-__device__ void block_stats(long long& a, int& b, int& c, PlanSmem& s) {
+// row_groups(L, c) for 0 <= L < 2^31 and 1 <= c < 2^16 with a reciprocal instead of
+// a division (division by an invariant integer: m = floor((2^32 - 1) / c) makes
+// floor(n * m / 2^32) low by at most one, which one compare corrects).
+struct Divider {
+  uint32_t d, m;
+  __device__ explicit Divider(int c) : d((uint32_t)c), m(0xFFFFFFFFu / (uint32_t)c) {}
+  __device__ int groups(int L) const {
+    if (L <= (int)d) return 1;
+    const uint32_t n = (uint32_t)L + d - 1u;  // ceil(L / d) = floor(n / d)
+    uint32_t q = __umulhi(n, m);
+    if (n - q * d >= d) ++q;
+    return (int)q;
+  }
+};
+
+// The block-wide helpers stay out of line: the planner runs once per batch from a cold
+// instruction cache, so one shared copy of each costs less than inlined copies.
+__device__ __noinline__ void block_stats(long long& a, int& b, int& c, PlanSmem& s) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   long long aa = a;
   int bb = b, cc = c;
@@ -69,8 +91,20 @@ __device__ void block_stats(long long& a, int& b, int& c, PlanSmem& s) {
   c = tc;
 }
 
+__device__ __noinline__ int block_min(int v, PlanSmem& s) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) s.red[2][w] = v;
+  __syncthreads();
+  int m = s.red[2][0];
+#pragma unroll
+  for (int i = 1; i < kPlanWarps; ++i) m = min(m, s.red[2][i]);
+  __syncthreads();
+  return m;
+}
+
 // Exclusive scan of one int per thread; the block total goes to *total.
-__device__ int block_scan(int v, int* total, PlanSmem& s) {
+__device__ __noinline__ int block_scan(int v, int* total, PlanSmem& s) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int x = v;
   for (int o = 1; o < 32; o <<= 1) {
@@ -90,6 +124,73 @@ __device__ int block_scan(int v, int* total, PlanSmem& s) {
   return before + x - v;
 }
 
+// CTAs of the multi-CTA rows at chunk c, one thread over every row (small batches).
+__device__ long long slots_serial(const int32_t* L_, int rows, int max_len, int c) {
+  const Divider dv(c);
+  long long n = 0;
+  for (int r = 0; r < rows; ++r) {
+    const int G = dv.groups(valid_len(L_[r], max_len));
+    if (G > 1) n += G;
+  }
+  return n;
+}
+
+// The same, rows spread over the block.
+__device__ long long slots_block(const int32_t* L_, int rows, int max_len, int c, PlanSmem& s) {
+  const Divider dv(c);
+  long long n = 0;
+  int b = 0, m = 0;
+  for (int r = threadIdx.x; r < rows; r += kPlanThreads) {
+    const int G = dv.groups(valid_len(L_[r], max_len));
+    if (G > 1) n += G;
+  }
+  block_stats(n, b, m, s);
+  return n;
+}
+
+// Automatic chunk (plan_logic.cuh, auto_chunk_ref): the smallest multiple of
+// kChunkAlign >= c0 whose multi-CTA rows fit the grid; kChunkCap when none does
+// (*fits = false). The CTA count only falls as c grows, so the first passing
+// candidate is the answer: up to kCandidateRows rows, 256 candidates spanning
+// [c0, kChunkCap] are tried at once and the step before the first pass is refined;
+// larger batches bisect.
+__device__ int auto_chunk(const int32_t* L_, int rows, int max_len, int grid, long long total,
+                          bool* fits, PlanSmem& s) {
+  const int c0 = initial_chunk(total, grid, 0);
+  const int tid = threadIdx.x;
+  *fits = true;
+  if (rows <= kCandidateRows) {
+    int step = (kChunkCap - c0 + kPlanThreads - 2) / (kPlanThreads - 1);
+    step = max(kChunkAlign, (step + kChunkAlign - 1) / kChunkAlign * kChunkAlign);
+    const int ct = min(c0 + step * tid, kChunkCap);
+    const int first = block_min(slots_serial(L_, rows, max_len, ct) <= grid ? tid : INT_MAX, s);
+    if (first == INT_MAX) {
+      *fits = false;
+      return kChunkCap;
+    }
+    if (first == 0) return c0;
+    const int lo = c0 + step * (first - 1);          // fails
+    const int hi = min(c0 + step * first, kChunkCap);  // passes
+    const int n2 = (hi - lo) / kChunkAlign;            // lo + 16, ..., hi
+    const int c2 = lo + kChunkAlign * (tid + 1);
+    const bool ok2 = tid < n2 && slots_serial(L_, rows, max_len, c2) <= grid;
+    const int f2 = block_min(ok2 ? tid : INT_MAX, s);
+    return lo + kChunkAlign * (f2 + 1);
+  }
+  if (slots_block(L_, rows, max_len, c0, s) <= grid) return c0;
+  if (slots_block(L_, rows, max_len, kChunkCap, s) > grid) {
+    *fits = false;
+    return kChunkCap;
+  }
+  int lo = c0, hi = kChunkCap;  // lo fails, hi passes
+  while (hi - lo > kChunkAlign) {
+    const int mid = lo + (hi - lo) / (2 * kChunkAlign) * kChunkAlign;
+    if (slots_block(L_, rows, max_len, mid, s) <= grid) hi = mid;
+    else lo = mid;
+  }
+  return hi;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ lens,
                                                             int rows, int max_len, int grid,
                                                             int chunk_force, char* ws) {
@@ -102,13 +203,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
   TOPK_MARK(g_plan_trace, 0);
   if (blockIdx.x > 0) {
-    // Clear every group state (the select kernel's counters and histograms).
-    uint4* g = reinterpret_cast<uint4*>(ws + lay.groups);
-    const size_t n16 = sizeof(GroupState) * (size_t)lay.ngroups / 16;
+    // Clear what the select kernel needs at zero in every group state: barrier
+    // flags, boundary-key AND/OR and histograms (the candidate lists are always
+    // written before they are read).
+    constexpr size_t kZeroBytes = offsetof(GroupState, cand_key);
+    static_assert(kZeroBytes % 16 == 0 && sizeof(GroupState) % 16 == 0, "zeroing granularity");
+    char* g = ws + lay.groups;
+    constexpr uint32_t per = (uint32_t)(kZeroBytes / 16);
+    const uint32_t n16 = per * (uint32_t)lay.ngroups;  // < 2^23
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (size_t i = (size_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n16;
-         i += (size_t)(gridDim.x - 1) * blockDim.x)
-      g[i] = z;
+    for (uint32_t i = (blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n16;
+         i += (gridDim.x - 1) * blockDim.x) {
+      const uint32_t grp = i / per, off = i - grp * per;
+      reinterpret_cast<uint4*>(g + (size_t)grp * sizeof(GroupState))[off] = z;
+    }
     TOPK_MARK(g_plan_trace, 9);
     return;
   }
@@ -130,98 +238,154 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   TOPK_MARK(g_plan_trace, 1);
 
   const bool forced = chunk_force > 0;
-  int c = initial_chunk(total, grid, chunk_force);
-  int waves = 0, plan_error = 0;
-  PlanStats st{0, 0, 0};
-  for (int iter = 0; iter < 64; ++iter) {
-    long long slots = 0;
-    int nm = 0, mg = 0;
-    for (int r = tid; r < rows; r += kPlanThreads) {
-      const int G = row_groups(valid_len(L_[r], max_len), c);
-      if (G > 1) {
-        slots += G;
-        nm += 1;
-        mg = max(mg, G);
-      }
-    }
-    block_stats(slots, nm, mg, s);
-    st = PlanStats{slots, nm, mg};
-    if (nm <= lay.ngroups && mg <= grid) {
-      int base = 0;
-      for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
-        const int r = r0 + tid;
-        const int G = r < rows ? row_groups(valid_len(L_[r], max_len), c) : 1;
-        int tot;
-        const int off = block_scan(G > 1 ? 1 : 0, &tot, s);
-        if (G > 1) {
-          s.multi_rows[base + off] = r;
-          s.multi_g[base + off] = G;
-        }
-        base += tot;
-      }
-      __syncthreads();
-      if (tid == 0) s.bcast[0] = pack_waves(s.multi_g, nm, grid, s.multi_wave, s.multi_cta);
-      __syncthreads();
-      waves = s.bcast[0];
-    } else {
-      waves = kMaxWaves + 1;
-    }
-    const int nc = next_chunk(c, st, waves, grid, forced, lay.ngroups);
-    if (nc == c) break;
-    if (nc < 0) {
-      plan_error = 1;
-      break;
-    }
-    c = nc;
-  }
+  bool fits = false;
+  int c = forced ? initial_chunk(total, grid, chunk_force)
+                 : auto_chunk(L_, rows, max_len, grid, total, &fits, s);
   TOPK_MARK(g_plan_trace, 2);
 
-  // Static unit table: clear the used waves, then one descriptor per multi-CTA chunk.
-  const int wv = plan_error ? 0 : waves;
-  for (int i = tid; i < wv * kMaxGrid; i += kPlanThreads) units[i].row = -1;
-  for (int i = tid; i < kMaxGrid / 32; i += kPlanThreads) s.busy[i] = 0u;
-  __syncthreads();
-  if (!plan_error) {
-    for (int i = 0; i < st.n_multi; ++i) {
-      const int G = s.multi_g[i];
-      const int row = s.multi_rows[i];
-      const int L = valid_len(L_[row], max_len);
-      for (int j = tid; j < G; j += kPlanThreads) {
-        const int cta = s.multi_cta[i] + j;
-        units[(int64_t)s.multi_wave[i] * kMaxGrid + cta] = make_unit(row, L, j, G, i);
-        atomicOr(&s.busy[cta >> 5], 1u << (cta & 31));
+  int waves = 0, plan_error = 0, n_multi = 0;
+  if (!forced && fits) {
+    // One wave: a row's group index and first CTA are exclusive prefixes over the
+    // rows (at most grid CTAs in total, so both fit 16 bits).
+    const Divider dv(c);
+    int base_n = 0, base_g = 0;
+    for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
+      const int r = r0 + tid;
+      const int G = r < rows ? dv.groups(valid_len(L_[r], max_len)) : 1;
+      int tot;
+      const int off = block_scan(G > 1 ? ((1 << 16) | G) : 0, &tot, s);
+      if (G > 1) {
+        const int i = base_n + (off >> 16);
+        s.multi_rows[i] = r;
+        s.multi_g[i] = G;
+        s.multi_wave[i] = 0;
+        s.multi_cta[i] = base_g + (off & 0xFFFF);
       }
+      base_n += tot >> 16;
+      base_g += tot & 0xFFFF;
     }
+    n_multi = base_n;
+    waves = n_multi > 0 ? 1 : 0;
+  } else {
+    // Forced chunk, or rows that do not fit one wave even at kChunkCap: grow the
+    // chunk while the groups break a hard limit (next_chunk), packing the groups
+    // into waves greedily.
+    PlanStats st{0, 0, 0};
+    for (int iter = 0; iter < 64; ++iter) {
+      long long slots = 0;
+      int nm = 0, mg = 0;
+      const Divider dv(c);
+      for (int r = tid; r < rows; r += kPlanThreads) {
+        const int G = dv.groups(valid_len(L_[r], max_len));
+        if (G > 1) {
+          slots += G;
+          nm += 1;
+          mg = max(mg, G);
+        }
+      }
+      block_stats(slots, nm, mg, s);
+      st = PlanStats{slots, nm, mg};
+      if (nm <= lay.ngroups && mg <= grid) {
+        int base = 0;
+        for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
+          const int r = r0 + tid;
+          const int G = r < rows ? dv.groups(valid_len(L_[r], max_len)) : 1;
+          int tot;
+          const int off = block_scan(G > 1 ? 1 : 0, &tot, s);
+          if (G > 1) {
+            s.multi_rows[base + off] = r;
+            s.multi_g[base + off] = G;
+          }
+          base += tot;
+        }
+        __syncthreads();
+        if (tid == 0) s.bcast[0] = pack_waves(s.multi_g, nm, grid, s.multi_wave, s.multi_cta);
+        __syncthreads();
+        waves = s.bcast[0];
+      } else {
+        waves = kMaxWaves + 1;
+      }
+      const int nc = next_chunk(c, st, waves, grid, forced, lay.ngroups);
+      if (nc == c) break;
+      if (nc < 0) {
+        plan_error = 1;
+        break;
+      }
+      c = nc;
+    }
+    n_multi = plan_error ? 0 : st.n_multi;
   }
+  __syncthreads();
   TOPK_MARK(g_plan_trace, 3);
 
+  // Static unit table for the grid's CTAs, one pass: CTA b of wave w runs the group
+  // whose CTA range holds it (groups are ordered by wave, then first CTA), else
+  // nothing. Two threads write the two 16-byte halves of one descriptor, so each
+  // warp stores 512 contiguous bytes.
+  const int wv = plan_error ? 0 : waves;
+  for (int i = tid; i < 2 * kMaxGrid; i += kPlanThreads) {
+    const int b = i >> 1;
+    if (b >= grid) break;
+    bool busy = false;
+    for (int w = 0; w < wv; ++w) {
+      int lo = 0, hi = n_multi - 1, f = -1;
+      while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s.multi_wave[mid] < w || (s.multi_wave[mid] == w && s.multi_cta[mid] <= b)) {
+          f = mid;
+          lo = mid + 1;
+        } else {
+          hi = mid - 1;
+        }
+      }
+      UnitDesc u{-1, 0, 0, 0, 0, 0, 0, 0};
+      if (f >= 0 && s.multi_wave[f] == w && b < s.multi_cta[f] + s.multi_g[f]) {
+        const int row = s.multi_rows[f];
+        u = make_unit(row, valid_len(L_[row], max_len), b - s.multi_cta[f], s.multi_g[f], f);
+        busy = true;
+      }
+      const uint4 half = (i & 1) ? make_uint4(u.rank, u.G, u.group, u.pad)
+                                 : make_uint4(u.row, u.s0, u.n, u.len);
+      reinterpret_cast<uint4*>(units + (int64_t)w * kMaxGrid + b)[i & 1] = half;
+    }
+    if ((i & 1) == 0) s.busy[b] = busy ? 1 : 0;
+  }
+  TOPK_MARK(g_plan_trace, 10);
+  __syncthreads();
+  TOPK_MARK(g_plan_trace, 4);
+
   // Row info.
+  const Divider dvc(c);
   for (int r = tid; r < rows; r += kPlanThreads) {
-    const int L = valid_len(L_[r], max_len);
     RowInfo x;
     x.len = L_[r];
-    x.G = plan_error ? 1 : row_groups(L, c);
+    x.G = plan_error ? 1 : dvc.groups(valid_len(L_[r], max_len));
     x.group = -1;
     x.pad = 0;
     ri[r] = x;
   }
   __syncthreads();
-  if (!plan_error)
-    for (int i = tid; i < st.n_multi; i += kPlanThreads) ri[s.multi_rows[i]].group = i;
-  TOPK_MARK(g_plan_trace, 4);
+  TOPK_MARK(g_plan_trace, 6);
+  for (int i = tid; i < n_multi; i += kPlanThreads) ri[s.multi_rows[i]].group = i;
 
   // Single-CTA rows, longest bucket first, row order inside a bucket.
   if (tid == 0) s.bucket_mask = 0u;
   __syncthreads();
   for (int r = tid; r < rows; r += kPlanThreads) {
     const int L = valid_len(L_[r], max_len);
-    if (plan_error || row_groups(L, c) == 1) atomicOr(&s.bucket_mask, 1u << len_bucket(L));
+    if (plan_error || dvc.groups(L) == 1) atomicOr(&s.bucket_mask, 1u << len_bucket(L));
   }
   __syncthreads();
+  TOPK_MARK(g_plan_trace, 7);
+#ifdef TOPK_TRACE
+  const long long ck0 = clock64();
+#endif
   const unsigned mask = s.bucket_mask;
   int n_single = 0;
-  for (int b = 31; b >= 0; --b) {
-    if (!(mask & (1u << b))) continue;
+#pragma unroll 1
+  for (unsigned m = mask; m != 0u; m &= ~(1u << (31 - __clz(m)))) {
+    const int b = 31 - __clz(m);  // present buckets, longest first
+#pragma unroll 1
     for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
       const int r = r0 + tid;
       bool take = false;
@@ -229,7 +393,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       if (r < rows) {
         Lraw = L_[r];
         const int L = valid_len(Lraw, max_len);
-        take = (plan_error || row_groups(L, c) == 1) && len_bucket(L) == b;
+        take = (plan_error || dvc.groups(L) == 1) && len_bucket(L) == b;
       }
       int tot;
       const int off = block_scan(take ? 1 : 0, &tot, s);
@@ -239,16 +403,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   }
 
   // One single row per CTA without static units, in CTA order.
+#ifdef TOPK_TRACE
+  const long long ck1 = clock64();
+  long long ck2 = 0, ck3 = 0;
+#endif
   int ordinal_base = 0;
   for (int c0 = 0; c0 < grid; c0 += kPlanThreads) {
     const int cta = c0 + tid;
-    const bool free_cta = cta < grid && !((s.busy[cta >> 5] >> (cta & 31)) & 1u);
+    const bool free_cta = cta < grid && !s.busy[cta];
     int tot;
     const int ord = ordinal_base + block_scan(free_cta ? 1 : 0, &tot, s);
-    if (cta < kMaxGrid) first_single[cta] = (free_cta && ord < n_single) ? ord : -1;
+#ifdef TOPK_TRACE
+    ck2 = clock64();
+#endif
+    if (cta < grid) first_single[cta] = (free_cta && ord < n_single) ? ord : -1;
     ordinal_base += tot;
+#ifdef TOPK_TRACE
+    ck3 = clock64();
+#endif
   }
+#ifdef TOPK_TRACE
+  if (tid == 0) {
+    g_plan_trace[11] = (uint64_t)(ck1 - ck0);
+    g_plan_trace[12] = (uint64_t)(ck2 - ck1);
+    g_plan_trace[13] = (uint64_t)(ck3 - ck2);
+    g_plan_trace[14] = (uint64_t)mask;
+  }
+#endif
   const int n_implicit = min(ordinal_base, n_single);
+  TOPK_MARK(g_plan_trace, 8);
 
   if (tid == 0) {
     h->magic = kMagic;
@@ -258,7 +441,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     h->chunk = c;
     h->waves = wv;
     h->n_single = n_single;
-    h->n_multi = plan_error ? 0 : st.n_multi;
+    h->n_multi = n_multi;
     h->status = plan_error ? TOPK_STATUS_PLAN_MISMATCH : 0;
     h->plan_error = plan_error;
     h->n_implicit = n_implicit;
@@ -281,8 +464,9 @@ extern "C" int topk_trace_plan(uint64_t* host, int n) {
 cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, int chunk_force,
                         void* ws, cudaStream_t stream) {
   const Layout lay = make_layout(rows);
-  const size_t bytes = sizeof(GroupState) * (size_t)lay.ngroups;
-  int zero_blocks = (int)((bytes / 16 + kPlanThreads * 16 - 1) / (kPlanThreads * 16));
+  const size_t n16 = offsetof(GroupState, cand_key) / 16 * (size_t)lay.ngroups;
+  const size_t per_block = (size_t)kPlanThreads * kZeroPerThread;
+  int zero_blocks = (int)((n16 + per_block - 1) / per_block);
   if (zero_blocks < 1) zero_blocks = 1;
   if (zero_blocks > 512) zero_blocks = 512;
   plan_kernel<<<1 + zero_blocks, kPlanThreads, 0, stream>>>(lens, rows, max_len, grid,
@@ -304,54 +488,79 @@ int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_fo
   long long total = 0;
   for (int r = 0; r < rows; ++r) total += valid_len(lens[r], max_len);
   const bool forced = chunk_force > 0;
+  auto slots_at = [&](int c) {
+    long long n = 0;
+    for (int r = 0; r < rows; ++r) {
+      const int G = row_groups(valid_len(lens[r], max_len), c);
+      if (G > 1) n += G;
+    }
+    return n;
+  };
   int c = initial_chunk(total, grid, chunk_force);
-  int waves = 0, plan_error = 0;
+  const bool fits = !forced && auto_chunk_ref(c, grid, slots_at, &c);
+  int waves = 0, plan_error = 0, n_multi = 0;
   static thread_local int32_t mr[kMaxGroups], mg[kMaxGroups], mw[kMaxGroups], mc[kMaxGroups];
-  PlanStats st{0, 0, 0};
-  for (int iter = 0; iter < 64; ++iter) {
-    st = PlanStats{0, 0, 0};
+  if (fits) {
+    int cta = 0;
     for (int r = 0; r < rows; ++r) {
       const int G = row_groups(valid_len(lens[r], max_len), c);
       if (G > 1) {
-        st.slots += G;
-        st.n_multi += 1;
-        if (G > st.max_g) st.max_g = G;
+        mr[n_multi] = r;
+        mg[n_multi] = G;
+        mw[n_multi] = 0;
+        mc[n_multi] = cta;
+        cta += G;
+        ++n_multi;
       }
     }
-    if (st.n_multi <= lay.ngroups && st.max_g <= grid) {
-      int n = 0;
+    waves = n_multi > 0 ? 1 : 0;
+  } else {
+    PlanStats st{0, 0, 0};
+    for (int iter = 0; iter < 64; ++iter) {
+      st = PlanStats{0, 0, 0};
       for (int r = 0; r < rows; ++r) {
         const int G = row_groups(valid_len(lens[r], max_len), c);
         if (G > 1) {
-          mr[n] = r;
-          mg[n] = G;
-          ++n;
+          st.slots += G;
+          st.n_multi += 1;
+          if (G > st.max_g) st.max_g = G;
         }
       }
-      waves = pack_waves(mg, n, grid, mw, mc);
-    } else {
-      waves = kMaxWaves + 1;
+      if (st.n_multi <= lay.ngroups && st.max_g <= grid) {
+        int n = 0;
+        for (int r = 0; r < rows; ++r) {
+          const int G = row_groups(valid_len(lens[r], max_len), c);
+          if (G > 1) {
+            mr[n] = r;
+            mg[n] = G;
+            ++n;
+          }
+        }
+        waves = pack_waves(mg, n, grid, mw, mc);
+      } else {
+        waves = kMaxWaves + 1;
+      }
+      const int nc = next_chunk(c, st, waves, grid, forced, lay.ngroups);
+      if (nc == c) break;
+      if (nc < 0) {
+        plan_error = 1;
+        break;
+      }
+      c = nc;
     }
-    const int nc = next_chunk(c, st, waves, grid, forced, lay.ngroups);
-    if (nc == c) break;
-    if (nc < 0) {
-      plan_error = 1;
-      break;
-    }
-    c = nc;
+    n_multi = plan_error ? 0 : st.n_multi;
   }
   const int wv = plan_error ? 0 : waves;
-  for (int i = 0; i < wv * kMaxGrid; ++i) units[i].row = -1;
+  for (int i = 0; i < wv * kMaxGrid; ++i) units[i] = UnitDesc{-1, 0, 0, 0, 0, 0, 0, 0};
   static thread_local uint8_t busy[kMaxGrid];
   for (int i = 0; i < kMaxGrid; ++i) busy[i] = 0;
-  if (!plan_error)
-    for (int i = 0; i < st.n_multi; ++i) {
-      const int L = valid_len(lens[mr[i]], max_len);
-      for (int j = 0; j < mg[i]; ++j) {
-        units[(int64_t)mw[i] * kMaxGrid + mc[i] + j] = make_unit(mr[i], L, j, mg[i], i);
-        busy[mc[i] + j] = 1;
-      }
+  for (int i = 0; i < n_multi; ++i) {
+    const int L = valid_len(lens[mr[i]], max_len);
+    for (int j = 0; j < mg[i]; ++j) {
+      units[(int64_t)mw[i] * kMaxGrid + mc[i] + j] = make_unit(mr[i], L, j, mg[i], i);
+      busy[mc[i] + j] = 1;
     }
+  }
   for (int r = 0; r < rows; ++r) {
     const int L = valid_len(lens[r], max_len);
     ri[r].len = lens[r];
@@ -359,8 +568,7 @@ int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_fo
     ri[r].group = -1;
     ri[r].pad = 0;
   }
-  if (!plan_error)
-    for (int i = 0; i < st.n_multi; ++i) ri[mr[i]].group = i;
+  for (int i = 0; i < n_multi; ++i) ri[mr[i]].group = i;
   int n_single = 0;
   for (int b = 31; b >= 0; --b)
     for (int r = 0; r < rows; ++r) {
@@ -385,7 +593,7 @@ int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_fo
   h->chunk = c;
   h->waves = wv;
   h->n_single = n_single;
-  h->n_multi = plan_error ? 0 : st.n_multi;
+  h->n_multi = n_multi;
   h->status = plan_error ? TOPK_STATUS_PLAN_MISMATCH : 0;
   h->plan_error = plan_error;
   h->n_implicit = n_implicit;

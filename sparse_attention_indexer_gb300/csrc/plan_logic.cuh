@@ -7,9 +7,11 @@
 //
 // Here the cutoff is a chunk size c (elements per CTA): rows with len <= c run on one
 // CTA (their row stays resident in that CTA's shared memory); longer rows are split
-// into G = ceil(len / c) CTAs that combine histograms through global memory. c starts
-// at ceil(total / grid) so the whole batch is spread evenly over the co-resident grid,
-// and grows while the multi-CTA groups do not fit one wave of the grid.
+// into G = ceil(len / c) CTAs that combine histograms through global memory. The
+// automatic c is the smallest multiple of kChunkAlign, at least c0 = ceil(total /
+// grid) (so the batch is spread evenly over the co-resident grid) and kMinAutoChunk,
+// whose multi-CTA rows fit one wave of the grid (auto_chunk_ref). A forced c grows
+// only while a hard limit is broken (next_chunk).
 #pragma once
 
 #include "common.cuh"
@@ -80,6 +82,30 @@ __host__ __device__ inline int next_chunk(int c, const PlanStats& s, int waves, 
   }
   if (!hard_ok && 2 * (int64_t)c > nc) nc = 2 * (int64_t)c;
   return round_chunk(nc);
+}
+
+// Automatic chunk: the smallest multiple of kChunkAlign in [c0, kChunkCap] with
+// slots_at(c) <= grid, where slots_at(c) counts the CTAs of the rows split at chunk c
+// (sum of G over rows with G > 1; it never grows with c, so bisection finds the
+// first pass). Returns false, with *c = kChunkCap, when not even kChunkCap fits.
+template <class SlotsAt>
+inline bool auto_chunk_ref(int c0, int grid, SlotsAt slots_at, int* c) {
+  if (slots_at(c0) <= grid) {
+    *c = c0;
+    return true;
+  }
+  if (slots_at(kChunkCap) > grid) {
+    *c = kChunkCap;
+    return false;
+  }
+  int lo = c0, hi = kChunkCap;  // lo fails, hi passes
+  while (hi - lo > kChunkAlign) {
+    const int mid = lo + (hi - lo) / (2 * kChunkAlign) * kChunkAlign;
+    if (slots_at(mid) <= grid) hi = mid;
+    else lo = mid;
+  }
+  *c = hi;
+  return true;
 }
 
 // Bucket of a single-CTA row for the longest-first claim order.

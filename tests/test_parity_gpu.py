@@ -209,10 +209,11 @@ def test_device_plan_matches_host_reference():
         assert np.array_equal(rd, rh)
         assert np.array_equal(sd[:hh["n_single"]], sh[:hh["n_single"]])
         assert np.array_equal(fd[:grid], fh[:grid])
-        nw = hh["waves"] * info["max_grid"]
-        used = uh[:nw, 0] >= 0
-        assert np.array_equal(ud[:nw, 0] >= 0, used)
-        assert np.array_equal(ud[:nw][used, :7], uh[:nw][used, :7])
+        # the select kernel reads the first `grid` descriptors of each wave
+        idx = (np.arange(hh["waves"])[:, None] * info["max_grid"] + np.arange(grid)).ravel()
+        used = uh[idx, 0] >= 0
+        assert np.array_equal(ud[idx, 0] >= 0, used)
+        assert np.array_equal(ud[idx][used, :7], uh[idx][used, :7])
 
 
 def test_status_errors():

@@ -215,3 +215,39 @@ def test_host_argument_errors():
     assert lib.topk_select_paged(2, 10, 4, 1, 10, 4, 4, 1, None, 64, 4, None, 256, None) == -8
     for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -11, 1, 16, 3):
         assert B.status_str(code)
+
+
+def _brute_auto_chunk(lens, max_len, grid, cap, align=16, min_auto=2048):
+    """Smallest multiple of `align` >= c0 whose split rows fit the grid, by linear scan."""
+    valid = [int(l) if 0 <= l <= max_len else 0 for l in lens]
+    c0 = max(-(-sum(valid) // grid), min_auto)
+    c0 = min(max(-(-c0 // align) * align, align), cap)
+
+    def slots(c):
+        return sum(-(-l // c) for l in valid if l > c)
+    for c in range(c0, cap + 1, align):
+        if slots(c) <= grid:
+            return c, True
+    return cap, False
+
+
+@pytest.mark.parametrize("grid", [152, 132, 37])
+def test_auto_chunk_is_smallest_fitting(grid):
+    """The automatic chunk is the smallest multiple of 16 (>= the even split of the
+    batch over the grid) at which the split rows need no more CTAs than the grid."""
+    _lib_or_skip()
+    cap = B.topk_chunk_capacity()
+    rng = np.random.default_rng(21)
+    cases = [W.verify_80k().lens, W.verify_1m().lens, W.mixed_decode().lens,
+             np.array([5000, 3, 70000, 12345], np.int32),
+             rng.integers(0, 200_000, size=9).astype(np.int32),
+             rng.integers(0, 60_000, size=300).astype(np.int32)]
+    for lens in cases:
+        max_len = int(max(lens.max(), 1))
+        hdr, _ = check_plan(lens, max_len, grid) if grid * cap >= max_len else (None, None)
+        if hdr is None:
+            continue
+        c, fits = _brute_auto_chunk(lens, max_len, grid, cap)
+        assert hdr["chunk"] == c, (lens[:8], hdr["chunk"], c)
+        if fits:
+            assert hdr["waves"] <= 1
