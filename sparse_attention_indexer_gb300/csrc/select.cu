@@ -259,7 +259,8 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 // flight). Thread 0 arrives by a release store of its rank's flag, (barriers passed)
 // << 32 | payload; the lanes of warp 0 acquire every rank's flag. Afterwards s.pay[j]
 // holds rank j's payload and *prefix (if non-null) the sum of the payloads of ranks
-// below this one. Returns false if a bounded wait expired (status set).
+// below this one, and s.bc[18] the largest payload. Returns false if a bounded wait
+// expired (status set).
 __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
   if (wrote) __threadfence();
   __syncthreads();
@@ -272,6 +273,7 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
     }
     __syncwarp();
     int acc = 0;
+    uint32_t mx = 0u;
     bool ok = true;
     int stuck = -1;
     for (int j = threadIdx.x; j < u.G && ok; j += 32) {
@@ -288,10 +290,14 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
       }
       c.s.pay[j] = (uint32_t)v;
       if (j < u.rank) acc += (int)(uint32_t)v;
+      mx = max(mx, (uint32_t)v);
     }
     const bool all_ok = __all_sync(0xffffffffu, ok);
 #pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int o = 16; o; o >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
     if (!ok) {
       set_status(c.h, TOPK_STATUS_TIMEOUT);
       record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, stuck, (int)my);
@@ -299,6 +305,7 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
     if (threadIdx.x == 0) {
       c.s.bc[15] = all_ok ? 1 : 0;
       c.s.bc[17] = acc;
+      c.s.bc[18] = (int)mx;
     }
   }
   __syncthreads();
@@ -418,6 +425,74 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
     for (int j = 0; j < 8; ++j) glob[j] = loc[j];
   }
   find_threshold(glob, loc, need, s);
+  b = s.bc[0];
+  above = s.bc[1];
+  eq = s.bc[2];
+  local_above = s.bc[3];
+  local_eq = s.bc[4];
+  __syncthreads();
+  return true;
+}
+
+// Level-0 threshold of the unit's row from the coarse histogram in s.u.hist (complete
+// for the chunk). A single-CTA row searches it directly. A CTA of a multi-CTA row
+// publishes only the bins at or above its own bin for `est` values, est = 4k/G (the
+// row's k values spread over G chunks), and sends that bin as its barrier payload.
+// The row histogram is then complete at bins >= the highest payload, B; if at least
+// `need` values lie there, the row's threshold is found exactly. Otherwise every CTA
+// publishes the bins it held back and the row meets once more. Outputs as
+// reduce_and_find; false on timeout.
+__device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int& local_above,
+                              int& local_eq) {
+  Smem& s = c.s;
+  const int need = u.kr;
+  const int t = threadIdx.x * 8;
+  uint32_t loc[8], glob[8];
+  load8(&s.u.hist[t], loc);
+  if (u.G == 1) {
+    find_threshold(loc, loc, need, s);
+  } else {
+    const int est = min(need, (int)((4ll * need + u.G - 1) / u.G));
+    int blocal = 0;
+    if (u.n >= est) {
+      find_threshold(loc, loc, est, s);
+      blocal = s.bc[0];
+      __syncthreads();
+    }
+    u.blocal = blocal;
+    bool wrote = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (loc[j] && t + j >= blocal) {
+        red_add_u32(&u.gs->hist0[t + j], loc[j]);
+        wrote = true;
+      }
+    if (!group_sync(c, u, wrote, (uint32_t)blocal, nullptr)) return false;
+    const int top = s.bc[18];
+    if (t + 7 >= blocal) {
+      load8_cg(&u.gs->hist0[t], glob);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) glob[j] = 0u;
+    }
+    if (threadIdx.x == 0) s.bc[0] = -1;
+    find_threshold(glob, loc, need, s);  // leaves s.bc[0] = -1 when not found
+    const bool complete = s.bc[0] >= top;
+    __syncthreads();
+    if (!complete) {
+      wrote = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (loc[j] && t + j < blocal) {
+          red_add_u32(&u.gs->hist0[t + j], loc[j]);
+          wrote = true;
+        }
+      u.blocal = 0;
+      if (!group_sync(c, u, wrote, 0u, nullptr)) return false;
+      load8_cg(&u.gs->hist0[t], glob);
+      find_threshold(glob, loc, need, s);
+    }
+  }
   b = s.bc[0];
   above = s.bc[1];
   eq = s.bc[2];
@@ -908,9 +983,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
 
   int b0, above0, eq0, la0, le0;
   u.blocal = 0;
-  if (!reduce_and_find(c, u, u.G > 1 ? u.gs->hist0 : nullptr, u.kr, u.n, true, b0, above0, eq0,
-                       la0, le0))
-    return;
+  if (!coarse_reduce(c, u, b0, above0, eq0, la0, le0)) return;
   TOPK_MARK(g_select_trace, 3);
   TOPK_LOG(u.r, 3);
   const int need = u.kr - above0;

@@ -280,3 +280,36 @@ def test_cuda_graph_replay():
     torch.cuda.synchronize()
     assert core.status() == 0
     compare_with_oracle(b, b.k, out.cpu().numpy(), pos.cpu().numpy())
+
+
+def test_skewed_rows_over_many_ctas():
+    """Rows whose top values are not spread evenly over the CTAs that share them:
+    sorted descending (one chunk holds the whole top-k, so the bins each CTA publishes
+    first cannot fix the threshold and the row publishes the rest), sorted ascending,
+    a step at 10 % of the row, shuffled sorted blocks and massive ties. Single-CTA and
+    multi-CTA splits, every k class."""
+    rng = np.random.default_rng(17)
+    L = 160000
+    base = rng.standard_normal(L).astype(np.float32)
+    desc = np.sort(base)[::-1].copy()
+    asc = np.sort(base).copy()
+    step = base.copy()
+    step[: L // 10] += 5.0
+    blocks = np.sort(base).reshape(40, -1)[rng.permutation(40)].ravel().copy()
+    ties = rng.integers(-2, 3, L).astype(np.float32)
+    s = np.stack([desc, asc, step, blocks, ties])
+    lens = np.array([L, L - 5, L - 17, L, L], np.int32)
+    tab = np.stack([rng.permutation(L // 64 + 1).astype(np.int32) for _ in range(5)])
+    b = W.Batch("sampled", s, lens, L, 2048, tab, None, 64)
+    for chunk in (16384, 20000, 48128):
+        for k in (1, 100, 2048):
+            slots, pos, st = run_gpu(b, k=k, chunk=chunk)
+            assert st == 0, B.status_str(st)
+            compare_with_oracle(b, k, slots, pos)
+    # one CTA per row
+    one = W.Batch("sampled1", s[:, :40000].copy(), np.full(5, 40000, np.int32), 40000, 2048,
+                  tab[:, :626].copy(), None, 64)
+    for k in (1, 100, 2048):
+        slots, pos, st = run_gpu(one, k=k, chunk=48128)
+        assert st == 0
+        compare_with_oracle(one, k, slots, pos)
