@@ -68,7 +68,8 @@ enum {
   TOPK_STATUS_TABLE_ENTRY = 4,    /* a selected position's table entry is negative: that entry -1 */
   TOPK_STATUS_SLOT_OVERFLOW = 8,  /* a slot exceeds INT32_MAX: that entry -1 */
   TOPK_STATUS_TIMEOUT = 16,       /* a bounded cross-CTA wait expired: row contents undefined */
-  TOPK_STATUS_PLAN_MISMATCH = 32  /* lens/rows/max_len differ from the plan, or no plan: rows -1 */
+  TOPK_STATUS_PLAN_MISMATCH = 32, /* lens/rows/max_len differ from the plan, or no plan: rows -1 */
+  TOPK_STATUS_ORDER = 64          /* a row barrier found a CTA already past it: row contents undefined */
 };
 
 #define TOPK_MAX_K 2048

@@ -24,6 +24,7 @@ STATUS_TABLE_ENTRY = 4
 STATUS_SLOT_OVERFLOW = 8
 STATUS_TIMEOUT = 16
 STATUS_PLAN_MISMATCH = 32
+STATUS_ORDER = 64
 ERR_STATIC_ROWS = -12
 STATIC_MAX_ROWS = 64
 

@@ -188,6 +188,7 @@ const char* topk_status_str(int code) {
       case TOPK_STATUS_SLOT_OVERFLOW: return "device: a slot exceeds INT32_MAX";
       case TOPK_STATUS_TIMEOUT: return "device: a bounded cross-CTA wait expired";
       case TOPK_STATUS_PLAN_MISMATCH: return "device: the plan does not match the call";
+      case TOPK_STATUS_ORDER: return "device: a row barrier found a CTA already past it";
       default: return "device: several status bits are set";
     }
   }

@@ -274,7 +274,7 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
     __syncwarp();
     int acc = 0;
     uint32_t mx = 0u;
-    bool ok = true;
+    bool ok = true, overrun = false;
     int stuck = -1;
     for (int j = threadIdx.x; j < u.G && ok; j += 32) {
       unsigned long long v = ld_acquire_u64(&u.gs->flag[j]);
@@ -288,11 +288,16 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
           }
         }
       }
+      // A rank already past this barrier has replaced its payload: the call's result
+      // would be undefined, so it is reported (it needs a waiter to stall for longer
+      // than a rank's work between two barriers).
+      if ((uint32_t)(v >> 32) != my) overrun = true;
       c.s.pay[j] = (uint32_t)v;
       if (j < u.rank) acc += (int)(uint32_t)v;
       mx = max(mx, (uint32_t)v);
     }
     const bool all_ok = __all_sync(0xffffffffu, ok);
+    if (__any_sync(0xffffffffu, overrun) && threadIdx.x == 0) set_status(c.h, TOPK_STATUS_ORDER);
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       acc += __shfl_xor_sync(0xffffffffu, acc, o);
