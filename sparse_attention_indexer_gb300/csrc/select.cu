@@ -619,6 +619,10 @@ __device__ void histogram_chunk(Ctx& c, Unit& u) {
   __syncthreads();
 }
 
+__device__ __forceinline__ float vmax4(const float4& x) {
+  return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+}
+
 // ------------------------------------------------------------- boundary selection
 
 // Exact selection among n <= kRankMax candidates: candidate i is taken iff fewer
@@ -1016,8 +1020,10 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const float thi = exact ? skip_below((uint32_t)b0 + 1u) : 0.0f;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   uint32_t fa = 0xFFFFFFFFu, fo = 0u;
-  int na = 0, nc = 0;
-  int hv0 = -1, hv1 = -1, hv2 = -1, hv3 = -1, nhv = 0;
+  int na = 0, nc = 0, nhv = 0;
+  // Vectors holding values to stage, newest first, 16 bits each (nvec < 2^16); the
+  // write step below revisits them when a thread has at most four.
+  unsigned long long hvs = 0ull;
   // classify one value: 0 below, 1 above (staged position), 2 boundary candidate
   auto klass = [&](float x) -> int {
     if (exact) return x >= tlo ? ((x >= thi || all_eq) ? 1 : 2) : 0;
@@ -1025,15 +1031,37 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     if (dg < (uint32_t)b0) return 0;
     return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
   };
-  auto count = [&](int v, const float4& x) {
-    const int e0 = 4 * v - u.head;
-    int a = 0, cd = 0;
-    if (exact && e0 >= 0 && e0 + 3 < u.n) {
-      // full vector, exact bin bounds: branch-free
-      const int ge = (x.x >= tlo) + (x.y >= tlo) + (x.z >= tlo) + (x.w >= tlo);
-      a = all_eq ? ge : (x.x >= thi) + (x.y >= thi) + (x.z >= thi) + (x.w >= thi);
-      cd = ge - a;
-    } else {
+  auto ge4 = [](const float4& x, float t) {
+    return (x.x >= t) + (x.y >= t) + (x.z >= t) + (x.w >= t);
+  };
+  if (exact) {
+    // Branch-free over every vector (shared-memory bound): exact counts from two
+    // compares per value. The chunk's first and last vectors mask the values outside
+    // it (to -inf, below tlo >= 0).
+    const int vfull0 = (u.head + 3) >> 2, vfull1 = (u.head + u.n) >> 2;
+    for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+      float4 x = b4[v];
+      if (v < vfull0 || v >= vfull1) {
+        const int e0 = 4 * v - u.head;
+        const float ninf = __int_as_float(0xFF800000);
+        if (e0 < 0 || e0 >= u.n) x.x = ninf;
+        if (e0 + 1 < 0 || e0 + 1 >= u.n) x.y = ninf;
+        if (e0 + 2 < 0 || e0 + 2 >= u.n) x.z = ninf;
+        if (e0 + 3 < 0 || e0 + 3 >= u.n) x.w = ninf;
+      }
+      const int g = ge4(x, tlo);
+      const int a = all_eq ? g : ge4(x, thi);
+      na += a;
+      nc += g - a;
+      const bool h = g > 0;
+      hvs = h ? ((hvs << 16) | (unsigned long long)v) : hvs;
+      nhv += h ? 1 : 0;
+    }
+    if (!stage_cand) nc = 0;
+  } else {
+    auto count = [&](int v, const float4& x) {
+      const int e0 = 4 * v - u.head;
+      int a = 0, cd = 0;
       const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -1051,36 +1079,17 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
           }
         }
       }
-    }
-    if (!stage_cand) cd = 0;
-    if (a + cd) {
-      na += a;
-      nc += cd;
-      if (nhv == 0) hv0 = v;
-      else if (nhv == 1) hv1 = v;
-      else if (nhv == 2) hv2 = v;
-      else if (nhv == 3) hv3 = v;
-      ++nhv;
-    }
-  };
-  {
-    auto vmax = [](const float4& x) { return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)); };
-    int v = threadIdx.x;
-    for (; v + 3 * kThreads < u.nvec; v += 4 * kThreads) {
-      const float4 x0 = b4[v], x1 = b4[v + kThreads];
-      const float4 x2 = b4[v + 2 * kThreads], x3 = b4[v + 3 * kThreads];
-      const bool h0 = !(vmax(x0) < tlo), h1 = !(vmax(x1) < tlo);
-      const bool h2 = !(vmax(x2) < tlo), h3 = !(vmax(x3) < tlo);
-      if (h0 | h1 | h2 | h3) {
-        if (h0) count(v, x0);
-        if (h1) count(v + kThreads, x1);
-        if (h2) count(v + 2 * kThreads, x2);
-        if (h3) count(v + 3 * kThreads, x3);
+      if (!stage_cand) cd = 0;
+      if (a + cd) {
+        na += a;
+        nc += cd;
+        hvs = (hvs << 16) | (unsigned long long)v;
+        ++nhv;
       }
-    }
-    for (; v < u.nvec; v += kThreads) {
+    };
+    for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
       const float4 x0 = b4[v];
-      if (!(vmax(x0) < tlo)) count(v, x0);
+      if (!(vmax4(x0) < tlo)) count(v, x0);
     }
   }
 #ifdef TOPK_TRACE
@@ -1128,10 +1137,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       }
     };
     if (nhv <= 4) {
-      write(hv0);
-      if (nhv >= 2) write(hv1);
-      if (nhv >= 3) write(hv2);
-      if (nhv >= 4) write(hv3);
+      for (int i = 0; i < nhv; ++i) write((int)((hvs >> (16 * i)) & 0xFFFFu));
     } else {
       for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
         const float4 x = b4[v];
