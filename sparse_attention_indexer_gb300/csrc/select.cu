@@ -208,6 +208,9 @@ __device__ void record_timeout(Header* h, int kind, int row, int rank, int seq, 
 struct Unit {
   int r, rank, G, L, kr, t, s0, n, head, nvec, npieces;
   int blocal;  // lowest coarse bin this CTA published to the row histogram
+  int issued;  // pieces of the chunk whose copies were issued
+  const char* src;  // the chunk's aligned source and its size in bytes
+  uint32_t bytes;
   GroupState* gs;
   uint32_t bar_seq;    // barriers passed in this unit
   uint32_t flag_base;  // barriers this rank had passed before this unit
@@ -522,15 +525,23 @@ __device__ __forceinline__ uint32_t chunk_geometry(const SelectParams& P, Unit& 
   u.head = (int)((A - A0) >> 2);
   u.nvec = (int)(bytes >> 4);
   u.npieces = (int)((bytes + kPieceBytes - 1) / kPieceBytes);
-  *src_aligned = reinterpret_cast<const char*>(A0);
+  u.src = reinterpret_cast<const char*>(A0);
+  u.bytes = bytes;
+  *src_aligned = u.src;
   return bytes;
 }
 
-// Bulk copies of the chunk, one per 16 KB piece, each completing on its mbarrier.
-// Called by one thread after the previous unit's shared-memory accesses completed.
-__device__ void issue_copies(Smem& s, const char* src, uint32_t bytes, int npieces) {
-  fence_proxy_async_smem();
-  for (int i = 0; i < npieces; ++i) {
+// Bulk copies of pieces [first, first + count) of the chunk, one per 16 KB piece,
+// each completing on its mbarrier. Called by one thread; the first call of a unit
+// comes after the previous unit's shared-memory accesses completed. At most kWindow
+// pieces are in flight: the copy engine interleaves outstanding copies, so with every
+// piece issued at once they all complete near the end; a window makes them land in
+// order, and pass 1 follows them.
+constexpr int kWindow = 4;
+
+__device__ void issue_copies(Smem& s, const char* src, uint32_t bytes, int first, int count) {
+  if (first == 0) fence_proxy_async_smem();
+  for (int i = first; i < first + count; ++i) {
     const uint32_t off = (uint32_t)i * kPieceBytes;
     const uint32_t sz = min((uint32_t)kPieceBytes, bytes - off);
     mbar_arrive_expect_tx(&s.mbar[i], sz);
@@ -541,7 +552,8 @@ __device__ void issue_copies(Smem& s, const char* src, uint32_t bytes, int npiec
 __device__ void issue_chunk(Ctx& c, Unit& u) {
   const char* src;
   const uint32_t bytes = chunk_geometry(c.p, u, &src);
-  if (threadIdx.x == 0) issue_copies(c.s, src, bytes, u.npieces);
+  u.issued = min(kWindow, u.npieces);
+  if (threadIdx.x == 0) issue_copies(c.s, src, bytes, 0, u.issued);
 }
 
 __device__ __forceinline__ void wait_piece(Ctx& c, int i) {
@@ -559,62 +571,43 @@ __device__ __forceinline__ void wait_piece(Ctx& c, int i) {
 // Waits for every piece of the unit (used when a unit is abandoned after its copies
 // were issued: shared memory must not be reused while copies are in flight).
 __device__ void drain_chunk(Ctx& c, Unit& u) {
-  for (int i = 0; i < u.npieces; ++i) wait_piece(c, i);
+  for (int i = 0; i < u.issued; ++i) wait_piece(c, i);
   __syncthreads();
 }
 
 // Builds the coarse histogram of the chunk in s.u.hist (zeroed by the caller before
-// the CTA barrier that precedes this call) while the pieces land. Each thread walks
-// its vectors (stride kThreads) and waits on a piece's mbarrier only when it first
-// reaches a vector of that piece; no warp-synchronous step in the loop.
+// the CTA barrier that precedes this call) piece by piece as the pieces land: every
+// thread waits on piece p, thread 0 then issues piece p + kWindow, and each thread
+// counts its (at most two) vectors of piece p.
 __device__ void histogram_chunk(Ctx& c, Unit& u) {
   Smem& s = c.s;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   constexpr int kVecPerPiece = kPieceBytes / 16;
-  int landed = 0;        // pieces this thread has seen complete
-  int landed_end = 0;    // vectors below this index have landed
-#ifdef TOPK_TRACE
-  uint64_t waited = 0;
-#endif
-  auto ensure = [&](int v) {
-    while (v >= landed_end && landed < u.npieces) {
-#ifdef TOPK_TRACE
-      const uint64_t w0 = global_timer_ns();
-#endif
-      wait_piece(c, landed);
-#ifdef TOPK_TRACE
-      waited += global_timer_ns() - w0;
-#endif
-      ++landed;
-      landed_end += kVecPerPiece;
-    }
-  };
   const int vfull0 = (u.head + 3) >> 2;  // first vector holding only chunk elements
   const int vfull1 = (u.head + u.n) >> 2;
-  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-    ensure(v);
-    const float4 x = b4[v];
-    if (v >= vfull0 && v < vfull1) {
-      atomicAdd(&s.u.hist[coarse_digit(x.x)], 1u);
-      atomicAdd(&s.u.hist[coarse_digit(x.y)], 1u);
-      atomicAdd(&s.u.hist[coarse_digit(x.z)], 1u);
-      atomicAdd(&s.u.hist[coarse_digit(x.w)], 1u);
-    } else {  // first or last vector of the chunk
-      const int e0 = 4 * v - u.head;
-      const float xs[4] = {x.x, x.y, x.z, x.w};
+  for (int p = 0; p < u.npieces; ++p) {
+    wait_piece(c, p);
+    if (threadIdx.x == 0 && p + kWindow < u.npieces) issue_copies(s, u.src, u.bytes, p + kWindow, 1);
+    const int vend = min((p + 1) * kVecPerPiece, u.nvec);
+    for (int v = p * kVecPerPiece + threadIdx.x; v < vend; v += kThreads) {
+      const float4 x = b4[v];
+      if (v >= vfull0 && v < vfull1) {
+        atomicAdd(&s.u.hist[coarse_digit(x.x)], 1u);
+        atomicAdd(&s.u.hist[coarse_digit(x.y)], 1u);
+        atomicAdd(&s.u.hist[coarse_digit(x.z)], 1u);
+        atomicAdd(&s.u.hist[coarse_digit(x.w)], 1u);
+      } else {  // first or last vector of the chunk
+        const int e0 = 4 * v - u.head;
+        const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (e0 + j >= 0 && e0 + j < u.n) atomicAdd(&s.u.hist[coarse_digit(xs[j])], 1u);
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j >= 0 && e0 + j < u.n) atomicAdd(&s.u.hist[coarse_digit(xs[j])], 1u);
+      }
     }
   }
-  // Every thread must observe every issued piece (the mbarrier phases advance once
-  // per unit), including pieces past its last vector.
-  ensure(u.nvec > 0 ? u.npieces * kVecPerPiece - 1 : -1);
+  u.issued = u.npieces;
 #ifdef TOPK_TRACE
-  if (threadIdx.x == 0) {
-    g_select_trace[blockIdx.x * 32 + 10] = waited;
-    g_select_trace[blockIdx.x * 32 + 11] = global_timer_ns();
-  }
+  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 11] = global_timer_ns();
 #endif
   __syncthreads();
 }
@@ -927,6 +920,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   u.head = 0;
   u.nvec = 0;
   u.npieces = 0;
+  u.issued = 0;
   u.gs = (u.G > 1 && d.group >= 0)
              ? reinterpret_cast<GroupState*>(P.ws + make_layout(P.rows).groups) + d.group
              : nullptr;
@@ -942,6 +936,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     if (pre_issued) {
       const char* src;
       chunk_geometry(P, u, &src);
+      u.issued = min(kWindow, u.npieces);
     } else {
       issue_chunk(c, u);
     }
@@ -1366,7 +1361,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
       u.n = d.n;
       const char* src;
       const uint32_t bytes = chunk_geometry(p, u, &src);
-      issue_copies(s, src, bytes, u.npieces);
+      issue_copies(s, src, bytes, 0, min(kWindow, u.npieces));
       s.bc[19] = 1;
     }
   }
