@@ -70,7 +70,6 @@ struct __align__(16) Smem {
   uint64_t mbar[kPieces];
   int wsum[kWarps];
   int wsum2[kWarps];
-  unsigned long long wsum64[kWarps];
   uint32_t wand[kWarps];
   uint32_t wor[kWarps];
   int bc[32];
@@ -267,6 +266,9 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
   if (wrote) __threadfence();
   __syncthreads();
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0 && u.bar_seq == 0) g_select_trace[blockIdx.x * 32 + 26] = global_timer_ns();
+#endif
   u.bar_seq += 1;
   const uint32_t my = u.flag_base + u.bar_seq;
   if (threadIdx.x < 32) {
@@ -321,58 +323,53 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
   return c.s.bc[15] != 0;
 }
 
-__device__ __forceinline__ unsigned long long warp_incl_scan64(unsigned long long x) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  return x;
-}
-
 // Finds bin b of a 4096-bin histogram (8 bins per thread: row-wide counts g[], this
 // CTA's counts l[]) with above(b) < need <= above(b) + g[b], above(b) counting bins
-// > b. Writes s.bc[0..4] = (b, above, g[b], this CTA's count above b, l[b]) with one
-// scan of the packed (row, local) per-thread sums. Requires 1 <= need <= sum(g).
+// > b. Writes s.bc[0..4] = (b, above, g[b], this CTA's count above b, l[b]); nothing
+// is written when the histogram holds fewer than `need` values.
 __device__ void find_threshold(const uint32_t (&g)[8], const uint32_t (&l)[8], int need, Smem& s) {
+  // Two 32-bit scans (counts never exceed a row's length, < 2^31).
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  unsigned long long gs = 0, ls = 0;
+  int gs = 0, ls = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    gs += g[j];
-    ls += l[j];
+    gs += (int)g[j];
+    ls += (int)l[j];
   }
-  const unsigned long long v = (gs << 32) | ls;
-  const unsigned long long incl = warp_incl_scan64(v);
-  if (lane == 31) s.wsum64[w] = incl;
+  const int ig = warp_incl_scan(gs), il = warp_incl_scan(ls);
+  if (lane == 31) {
+    s.wsum[w] = ig;
+    s.wsum2[w] = il;
+  }
   __syncthreads();
-  unsigned long long before = 0, total = 0;
+  int bg = 0, tg = 0, bl = 0, tl = 0;
 #pragma unroll
   for (int i = 0; i < kWarps; ++i) {
-    const unsigned long long x = s.wsum64[i];
-    if (i < w) before += x;
-    total += x;
+    const int xg = s.wsum[i], xl = s.wsum2[i];
+    if (i < w) {
+      bg += xg;
+      bl += xl;
+    }
+    tg += xg;
+    tl += xl;
   }
-  const unsigned long long excl = before + incl - v;
   // counts owned by higher threads
-  const long long g_above = (long long)(total >> 32) - (long long)(excl >> 32) - (long long)gs;
-  const long long l_above = (long long)(total & 0xFFFFFFFFull) - (long long)(excl & 0xFFFFFFFFull) -
-                            (long long)ls;
-  if (g_above < need && need <= g_above + (long long)gs) {
-    long long cg = g_above, cl = l_above;
+  const int g_above = tg - (bg + ig);
+  const int l_above = tl - (bl + il);
+  if (g_above < need && need <= g_above + gs) {
+    int cg = g_above, cl = l_above;
 #pragma unroll
     for (int j = 7; j >= 0; --j) {
-      if (cg + (long long)g[j] >= need) {
+      if (cg + (int)g[j] >= need) {
         s.bc[0] = threadIdx.x * 8 + j;
-        s.bc[1] = (int)cg;
+        s.bc[1] = cg;
         s.bc[2] = (int)g[j];
-        s.bc[3] = (int)cl;
+        s.bc[3] = cl;
         s.bc[4] = (int)l[j];
         break;
       }
-      cg += g[j];
-      cl += l[j];
+      cg += (int)g[j];
+      cl += (int)l[j];
     }
   }
   __syncthreads();
@@ -468,6 +465,7 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
       __syncthreads();
     }
     u.blocal = blocal;
+    TOPK_MARK(g_select_trace, 24);
     bool wrote = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -475,7 +473,16 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
         red_add_u32(&u.gs->hist0[t + j], loc[j]);
         wrote = true;
       }
+#ifdef TOPK_TRACE
+    {
+      int nw = 0;
+      for (int j = 0; j < 8; ++j) nw += (loc[j] && t + j >= blocal) ? 1 : 0;
+      nw = __reduce_add_sync(0xffffffffu, nw);
+      if ((threadIdx.x & 31) == 0) atomicAdd(&s.bc[30], nw);
+    }
+#endif
     if (!group_sync(c, u, wrote, (uint32_t)blocal, nullptr)) return false;
+    TOPK_MARK(g_select_trace, 25);
     const int top = s.bc[18];
     if (t + 7 >= blocal) {
       load8_cg(&u.gs->hist0[t], glob);
@@ -942,6 +949,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     }
   }
   for (int i = threadIdx.x; i < kBins0; i += kThreads) s.u.hist[i] = 0u;
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0) s.bc[30] = 0;
+#endif
   TOPK_MARK(g_select_trace, 1);
 
   // Row-level checks against the call: every CTA of the row decides the same way.
@@ -989,6 +999,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   u.blocal = 0;
   if (!coarse_reduce(c, u, b0, above0, eq0, la0, le0)) return;
   TOPK_MARK(g_select_trace, 3);
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 28] = (uint64_t)s.bc[30] << 32;
+#endif
   TOPK_LOG(u.r, 3);
   const int need = u.kr - above0;
   const bool all_eq = (eq0 == need);
