@@ -222,6 +222,32 @@ struct Ctx {
   uint32_t mphase;  // parity bits of the piece mbarriers
 };
 
+// Physical slot of logical position p of the unit's row (-1 with a status bit for a
+// negative table entry or a slot above INT32_MAX).
+__device__ __forceinline__ int32_t lookup_slot(const Ctx& c, const Unit& u, int p) {
+  const SelectParams& P = c.p;
+  const int32_t page = __ldg(P.table + (int64_t)u.t * P.table_ld + p / P.page_size);
+  if (page < 0) {
+    set_status(c.h, TOPK_STATUS_TABLE_ENTRY);
+    return -1;
+  }
+  const int64_t sl = (int64_t)page * P.page_size + p % P.page_size;
+  if (sl > 0x7FFFFFFFll) {
+    set_status(c.h, TOPK_STATUS_SLOT_OVERFLOW);
+    return -1;
+  }
+  return (int32_t)sl;
+}
+
+// Writes position p with its slot at output index idx of the unit's row.
+__device__ __forceinline__ void put(const Ctx& c, const Unit& u, int idx, int p, int32_t slot) {
+  const SelectParams& P = c.p;
+  if ((unsigned)idx >= (unsigned)P.k) return;  // never taken
+  const int64_t o = (int64_t)u.r * P.k + idx;
+  P.out_slots[o] = slot;
+  if (P.out_pos) P.out_pos[o] = p;
+}
+
 // Writes one selected position p at output index idx of the unit's row.
 __device__ __forceinline__ void emit(const Ctx& c, const Unit& u, int idx, int p) {
   const SelectParams& P = c.p;
@@ -254,16 +280,17 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
   }
 }
 
-// Row barrier among the G CTAs of a row. All threads call it; a thread that wrote
-// row state to global memory (histogram reductions, candidates) passes wrote = true
-// and fences its own writes first, so that they are performed before thread 0
-// arrives (an arrival by one thread does not order other warps' writes still in
-// flight). Thread 0 arrives by a release store of its rank's flag, (barriers passed)
-// << 32 | payload; the lanes of warp 0 acquire every rank's flag. Afterwards s.pay[j]
-// holds rank j's payload and *prefix (if non-null) the sum of the payloads of ranks
-// below this one, and s.bc[18] the largest payload. Returns false if a bounded wait
-// expired (status set).
-__device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
+// Row barriers among the G CTAs of a row, as an arrival and a wait (a CTA can work
+// in between). All threads call both. At arrival, a thread that wrote row state to
+// global memory (histogram reductions, candidates) passes wrote = true and fences its
+// own writes first, so that they are performed before thread 0 arrives (an arrival by
+// one thread does not order other warps' writes still in flight); thread 0 then
+// release-stores its rank's flag, (barriers passed) << 32 | payload. The wait has the
+// lanes of warp 0 acquire every rank's flag; afterwards s.pay[j] holds rank j's
+// payload, *prefix (if non-null) the sum of the payloads of ranks below this one and
+// s.bc[18] the largest payload. group_wait returns false if a bounded wait expired
+// (status set).
+__device__ uint32_t group_arrive(Unit& u, bool wrote, uint32_t payload) {
   if (wrote) __threadfence();
   __syncthreads();
 #ifdef TOPK_TRACE
@@ -271,11 +298,15 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
 #endif
   u.bar_seq += 1;
   const uint32_t my = u.flag_base + u.bar_seq;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
+  }
+  return my;
+}
+
+__device__ bool group_wait(Ctx& c, Unit& u, uint32_t my, int* prefix) {
   if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) {
-      __threadfence();
-      st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
-    }
     __syncwarp();
     int acc = 0;
     uint32_t mx = 0u;
@@ -310,7 +341,7 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
     }
     if (!ok) {
       set_status(c.h, TOPK_STATUS_TIMEOUT);
-      record_timeout(c.h, 1, u.r, u.rank, (int)u.bar_seq, stuck, (int)my);
+      record_timeout(c.h, 1, u.r, u.rank, (int)(my - u.flag_base), stuck, (int)my);
     }
     if (threadIdx.x == 0) {
       c.s.bc[15] = all_ok ? 1 : 0;
@@ -321,6 +352,10 @@ __device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* p
   __syncthreads();
   if (prefix) *prefix = c.s.bc[17];
   return c.s.bc[15] != 0;
+}
+
+__device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
+  return group_wait(c, u, group_arrive(u, wrote, payload), prefix);
 }
 
 // Finds bin b of a 4096-bin histogram (8 bins per thread: row-wide counts g[], this
@@ -1218,36 +1253,59 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   };
   if (slots) write_candidates(u.rank * slot_cap);
 
-  // Row-wide offsets (G > 1): one barrier delivers every rank's counts (and the
-  // fallback's key AND/OR); each CTA then clears the histogram bins it published.
+  // Row-wide offsets (G > 1) come with one barrier that delivers every rank's counts;
+  // each CTA then clears the histogram bins it published. On the common path the
+  // slots of the staged positions and of this CTA's own candidates are looked up
+  // between its arrival and the wait (into the chunk buffer, free once pass 2 is
+  // done: the candidate gather below uses its first 2 * kGroupCap words), so that
+  // emitting after the barrier is stores only. The fallback's barrier also carries
+  // the boundary keys' AND/OR.
+  const uint32_t counts = (uint32_t)my_emit | ((uint32_t)my_cand << 16);
+  const int n_emit = min(s.bc[9], TOPK_MAX_K);
+  const int n_own = stage_cand ? min(s.bc[10], kListCap) : 0;
+  int32_t* slot_e = reinterpret_cast<int32_t*>(s.buf) + 2 * kGroupCap;  // [TOPK_MAX_K]
+  int32_t* slot_c = slot_e + TOPK_MAX_K;                                // [kListCap]
+  const bool overlap = u.G > 1 && !fallback && !(compact && !slots && !stage_cand);
   int out_base = 0, cand_base = 0;
-  if (u.G > 1) {
-    if (fallback && threadIdx.x == 0) {
-      atomicOr(&u.gs->and_key, ~fa);  // stored inverted so the reset value is 0
-      atomicOr(&u.gs->or_key, fo);
-    }
+  if (overlap) {
+    const uint32_t seq = group_arrive(u, wrote_cand, counts);
+    for (int i = threadIdx.x; i < n_emit; i += kThreads)
+      slot_e[i] = lookup_slot(c, u, s.u.l.elist[i]);
+    for (int i = threadIdx.x; i < n_own; i += kThreads)
+      slot_c[i] = lookup_slot(c, u, (int)s.u.l.cpos[i]);
     int pre;
-    if (!group_sync(c, u, wrote_cand || (fallback && threadIdx.x == 0),
-                    (uint32_t)my_emit | ((uint32_t)my_cand << 16), &pre))
-      return;
+    if (!group_wait(c, u, seq, &pre)) return;
     for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
     out_base = pre & 0xFFFF;
     cand_base = pre >> 16;
-    if (fallback) {
-      if (threadIdx.x == 0) {
-        s.bc[11] = (int)~__ldcg(&u.gs->and_key);
-        s.bc[12] = (int)__ldcg(&u.gs->or_key);
+    TOPK_MARK(g_select_trace, 5);
+    for (int i = threadIdx.x; i < n_emit; i += kThreads)
+      put(c, u, out_base + i, s.u.l.elist[i], slot_e[i]);
+  } else {
+    if (u.G > 1) {
+      if (fallback && threadIdx.x == 0) {
+        atomicOr(&u.gs->and_key, ~fa);  // stored inverted so the reset value is 0
+        atomicOr(&u.gs->or_key, fo);
       }
-      __syncthreads();
-      fa = (uint32_t)s.bc[11];
-      fo = (uint32_t)s.bc[12];
+      int pre;
+      if (!group_sync(c, u, wrote_cand || (fallback && threadIdx.x == 0), counts, &pre)) return;
+      for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
+      out_base = pre & 0xFFFF;
+      cand_base = pre >> 16;
+      if (fallback) {
+        if (threadIdx.x == 0) {
+          s.bc[11] = (int)~__ldcg(&u.gs->and_key);
+          s.bc[12] = (int)__ldcg(&u.gs->or_key);
+        }
+        __syncthreads();
+        fa = (uint32_t)s.bc[11];
+        fo = (uint32_t)s.bc[12];
+      }
     }
+    TOPK_MARK(g_select_trace, 5);
+    // Emit the staged positions (table lookups of the whole CTA in parallel).
+    for (int i = threadIdx.x; i < n_emit; i += kThreads) emit(c, u, out_base + i, s.u.l.elist[i]);
   }
-  TOPK_MARK(g_select_trace, 5);
-
-  // Emit the staged positions (table lookups of the whole CTA in parallel).
-  const int n_emit = min(s.bc[9], TOPK_MAX_K);
-  for (int i = threadIdx.x; i < n_emit; i += kThreads) emit(c, u, out_base + i, s.u.l.elist[i]);
 
   if (compact && u.G == 1) {
     __syncthreads();
@@ -1300,15 +1358,29 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     // The method must be the same in every CTA of the row (output index schemes
     // differ), so it depends on the row-wide count only.
     if (n <= kRankOwnMax) {
-      // rank this CTA's own candidates against all of them
-      for (int i = own0 + threadIdx.x; i < own1; i += kThreads) {
-        const uint32_t ki = lkey[i], pi = lpos[i];
+      // Rank this CTA's own candidates against all of them, T lanes per candidate
+      // (groups of T never straddle a warp); the own staged candidates' slots were
+      // looked up before the barrier.
+      const int m = own1 - own0;
+      const bool have_slots = overlap && stage_cand;
+      int T = 1;
+      while (T < 32 && m * (T * 2) <= kThreads) T *= 2;
+      const int sub = threadIdx.x & (T - 1);
+      for (int i0 = 0; i0 < m * T; i0 += kThreads) {
+        const int gi = (i0 + threadIdx.x) / T;
+        const bool act = gi < m;
+        const uint32_t ki = act ? lkey[own0 + gi] : 0u, pi = act ? lpos[own0 + gi] : 0u;
         int rank = 0;
-        for (int j = 0; j < n; ++j) {
-          const uint32_t kj = lkey[j], pj = lpos[j];
-          rank += (kj > ki || (kj == ki && pj < pi)) ? 1 : 0;
+        if (act)
+          for (int j = sub; j < n; j += T) {
+            const uint32_t kj = lkey[j], pj = lpos[j];
+            rank += (kj > ki || (kj == ki && pj < pi)) ? 1 : 0;
+          }
+        for (int o = 1; o < T; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (act && sub == 0 && rank < need) {
+          if (have_slots) put(c, u, above0 + rank, (int)pi, slot_c[gi]);
+          else emit(c, u, above0 + rank, (int)pi);
         }
-        if (rank < need) emit(c, u, above0 + rank, (int)pi);
       }
     } else {
       // radix-select among all candidates (same marks in every CTA), then each CTA
