@@ -191,6 +191,150 @@ __device__ int auto_chunk(const int32_t* L_, int rows, int max_len, int grid, lo
   return hi;
 }
 
+// Plan of a batch of at most 32 rows without a forced chunk: warp 0 decides (lane =
+// row: the chunk search tries 32 candidates per round, a ballot picks the first that
+// fits; group indices and first CTAs are warp scans), then the block writes the
+// tables. Same plan as the general path below (auto_chunk_ref's rule, one wave).
+// Returns false, with nothing written, when the rows do not fit one wave even at
+// kChunkCap (the general path then packs several waves).
+constexpr int kSmallRows = 32;
+
+__device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_len, int grid,
+                           char* ws, const Layout& lay, PlanSmem& s) {
+  Header* h = reinterpret_cast<Header*>(ws + lay.header);
+  RowInfo* ri = reinterpret_cast<RowInfo*>(ws + lay.rowinfo);
+  int2* singles = reinterpret_cast<int2*>(ws + lay.singles);
+  int32_t* first_single = reinterpret_cast<int32_t*>(ws + lay.first_single);
+  UnitDesc* units = reinterpret_cast<UnitDesc*>(ws + lay.units);
+  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr unsigned kAll = 0xffffffffu;
+  if (tid < 32) {
+    const int Lraw = lane < rows ? lens[lane] : 0;
+    const int L = lane < rows ? valid_len(Lraw, max_len) : 0;
+    long long tot = L;
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(kAll, tot, o);
+    // CTAs of the split rows at chunk cc (every lane evaluates its own cc)
+    auto slots_at = [&](int cc) {
+      const Divider dv(cc);
+      int n = 0;
+      for (int r = 0; r < rows; ++r) {
+        const int G = dv.groups(__shfl_sync(kAll, L, r));
+        n += G > 1 ? G : 0;
+      }
+      return n;
+    };
+    if (lane < rows) s.lens[lane] = L;
+    const int c0 = initial_chunk(tot, grid, 0);
+    // a fails (c0 may pass); b = kChunkCap passes unless no chunk fits, which the
+    // first round (lane 31 evaluates b) shows
+    int a = c0 - kChunkAlign, b = kChunkCap;
+    bool fits = true;
+    while (b - a > kChunkAlign) {
+      int step = (b - a + 31) / 32;
+      step = (step + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+      const int cand = min(a + step * (lane + 1), b);
+      const unsigned m = __ballot_sync(kAll, slots_at(cand) <= grid);
+      if (m == 0u) {
+        fits = false;
+        break;
+      }
+      const int first = __ffs(m) - 1;
+      const int nb = __shfl_sync(kAll, cand, first);
+      const int na = __shfl_sync(kAll, cand, max(first - 1, 0));
+      a = first == 0 ? a : na;
+      b = nb;
+    }
+    const int c = b;
+    if (lane == 0) s.bcast[4] = fits ? 1 : 0;
+    if (fits) {
+      const Divider dv(c);
+      const int G = lane < rows ? dv.groups(L) : 1;
+      const bool multi = G > 1;
+      const unsigned lt = (1u << lane) - 1u;
+      const unsigned mm = __ballot_sync(kAll, multi);
+      const int gi = __popc(mm & lt);
+      int incl = multi ? G : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kAll, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total_slots = __shfl_sync(kAll, incl, 31);
+      if (multi) {
+        s.multi_rows[gi] = lane;
+        s.multi_g[gi] = G;
+        s.multi_wave[gi] = 0;
+        s.multi_cta[gi] = incl - G;
+      }
+      if (lane < rows) {
+        RowInfo x;
+        x.len = Lraw;
+        x.G = G;
+        x.group = multi ? gi : -1;
+        x.pad = 0;
+        ri[lane] = x;
+      }
+      // single rows: longest length bucket first, row order inside a bucket
+      const bool single = lane < rows && !multi;
+      const int bucket = L > 0 ? 31 - __clz(L) : 0;
+      int rank = 0;
+      for (int j = 0; j < 32; ++j) {
+        const int bj = __shfl_sync(kAll, bucket, j);
+        const bool sj = __shfl_sync(kAll, single ? 1 : 0, j) != 0;
+        rank += (sj && (bj > bucket || (bj == bucket && j < lane))) ? 1 : 0;
+      }
+      const int n_single = __popc(__ballot_sync(kAll, single));
+      if (single) singles[rank] = make_int2(lane, Lraw);
+      const int n_multi = __popc(mm);
+      if (lane == 0) {
+        const int n_implicit = min(grid - total_slots, n_single);
+        h->magic = kMagic;
+        h->rows = rows;
+        h->max_len = max_len;
+        h->grid = grid;
+        h->chunk = c;
+        h->waves = n_multi > 0 ? 1 : 0;
+        h->n_single = n_single;
+        h->n_multi = n_multi;
+        h->status = 0;
+        h->plan_error = 0;
+        h->n_implicit = n_implicit;
+        h->dyn_period = n_single - n_implicit + grid;
+        h->steal = 0ull;
+        for (int i = 0; i < 8; ++i) h->diag[i] = 0;
+        s.bcast[0] = n_multi;
+        s.bcast[1] = total_slots;
+        s.bcast[2] = n_single;
+      }
+    }
+  }
+  __syncthreads();
+  if (!s.bcast[4]) return false;
+  const int n_multi = s.bcast[0], total_slots = s.bcast[1], n_single = s.bcast[2];
+  // Unit table of wave 0 for the grid's CTAs (two threads per descriptor, 16 bytes
+  // each: each warp stores 512 contiguous bytes); the first-single table in closed
+  // form (busy CTAs are [0, total_slots)).
+  for (int i = tid; i < 2 * grid; i += kPlanThreads) {
+    const int b = i >> 1;
+    UnitDesc u{-1, 0, 0, 0, 0, 0, 0, 0};
+    if (n_multi > 0 && b < total_slots) {
+      int lo = 0, hi = n_multi - 1;  // last group whose first CTA <= b
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.multi_cta[mid] <= b) lo = mid;
+        else hi = mid - 1;
+      }
+      const int row = s.multi_rows[lo];
+      u = make_unit(row, s.lens[row], b - s.multi_cta[lo], s.multi_g[lo], lo);
+    }
+    const uint4 half = (i & 1) ? make_uint4(u.rank, u.G, u.group, u.pad)
+                               : make_uint4(u.row, u.s0, u.n, u.len);
+    reinterpret_cast<uint4*>(units + b)[i & 1] = half;
+  }
+  for (int b = tid; b < grid; b += kPlanThreads)
+    first_single[b] = (b >= total_slots && b - total_slots < n_single) ? b - total_slots : -1;
+  return true;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ lens,
                                                             int rows, int max_len, int grid,
                                                             int chunk_force, char* ws) {
@@ -223,6 +367,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
   __shared__ PlanSmem s;
   const int tid = threadIdx.x;
+  if (chunk_force <= 0 && rows <= kSmallRows && plan_small(lens, rows, max_len, grid, ws, lay, s)) {
+    TOPK_MARK(g_plan_trace, 5);
+    return;
+  }
 
   // Lengths are read many times below: keep them in shared memory when they fit.
   const bool cached = rows <= kLensCache;

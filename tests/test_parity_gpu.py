@@ -196,7 +196,9 @@ def test_slots_only_output():
 def test_device_plan_matches_host_reference():
     from tests.test_plan_host import parse_plan
     grid = B.topk_grid_size()
-    for b in (W.verify_80k(), W.verify_1m(), W.mixed_decode(), W.adversarial()):
+    mixed = W.mixed_decode()
+    few = _subset(mixed, np.arange(20))  # <= 32 rows: the one-warp planner, both row kinds
+    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
