@@ -1064,9 +1064,11 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   uint32_t fa = 0xFFFFFFFFu, fo = 0u;
   int na = 0, nc = 0, nhv = 0;
-  // Vectors holding values to stage, newest first, 16 bits each (nvec < 2^16); the
-  // write step below revisits them when a thread has at most four.
-  unsigned long long hvs = 0ull;
+  // Vectors holding values to stage, newest first, 16 bits each (nvec < 2^16) in two
+  // words; the write step below revisits them when a thread has at most eight (a
+  // thread holds 0.8 such vectors on average on the 1M rows; more than eight would
+  // make it rescan the chunk while the CTA waits).
+  unsigned long long hvs = 0ull, hvs2 = 0ull;
   // classify one value: 0 below, 1 above (staged position), 2 boundary candidate
   auto klass = [&](float x) -> int {
     if (exact) return x >= tlo ? ((x >= thi || all_eq) ? 1 : 2) : 0;
@@ -1097,6 +1099,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       na += a;
       nc += g - a;
       const bool h = g > 0;
+      hvs2 = h ? ((hvs2 << 16) | (hvs >> 48)) : hvs2;
       hvs = h ? ((hvs << 16) | (unsigned long long)v) : hvs;
       nhv += h ? 1 : 0;
     }
@@ -1126,6 +1129,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       if (a + cd) {
         na += a;
         nc += cd;
+        hvs2 = (hvs2 << 16) | (hvs >> 48);
         hvs = (hvs << 16) | (unsigned long long)v;
         ++nhv;
       }
@@ -1179,8 +1183,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         }
       }
     };
-    if (nhv <= 4) {
-      for (int i = 0; i < nhv; ++i) write((int)((hvs >> (16 * i)) & 0xFFFFu));
+    if (nhv <= 8) {
+      for (int i = 0; i < nhv; ++i)
+        write((int)(((i < 4 ? hvs : hvs2) >> (16 * (i & 3))) & 0xFFFFu));
     } else {
       for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
         const float4 x = b4[v];
