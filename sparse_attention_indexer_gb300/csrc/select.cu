@@ -1279,13 +1279,25 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     for (int i = threadIdx.x; i < n_own; i += kThreads)
       slot_c[i] = lookup_slot(c, u, (int)s.u.l.cpos[i]);
     int pre;
+#ifdef TOPK_TRACE
+    const long long qa = clock64();
+#endif
     if (!group_wait(c, u, seq, &pre)) return;
-    for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
+#ifdef TOPK_TRACE
+    const long long qb = clock64();
+#endif
     out_base = pre & 0xFFFF;
     cand_base = pre >> 16;
     TOPK_MARK(g_select_trace, 5);
     for (int i = threadIdx.x; i < n_emit; i += kThreads)
       put(c, u, out_base + i, s.u.l.elist[i], slot_e[i]);
+#ifdef TOPK_TRACE
+    const long long qc = clock64();
+    if (threadIdx.x == 0) {
+      g_select_trace[blockIdx.x * 32 + 13] = (uint64_t)(qb - qa);
+      g_select_trace[blockIdx.x * 32 + 14] = (uint64_t)(qc - qb);
+    }
+#endif
   } else {
     if (u.G > 1) {
       if (fallback && threadIdx.x == 0) {
@@ -1359,6 +1371,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     }
     __syncthreads();
     TOPK_MARK(g_select_trace, 6);
+#ifdef TOPK_TRACE
+    const long long qd = clock64();
+#endif
     const int own0 = min(cand_base, n), own1 = min(cand_base + le0, n);
     // The method must be the same in every CTA of the row (output index schemes
     // differ), so it depends on the row-wide count only.
@@ -1387,6 +1402,20 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
           else emit(c, u, above0 + rank, (int)pi);
         }
       }
+#ifdef TOPK_TRACE
+      {
+        const long long qe = clock64();
+        __shared__ unsigned long long qmx;
+        if (threadIdx.x == 0) qmx = 0;
+        __syncthreads();
+        atomicMax(&qmx, (unsigned long long)(qe - qd));
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          g_select_trace[blockIdx.x * 32 + 15] = qmx;
+          g_select_trace[blockIdx.x * 32 + 31] = (uint64_t)m | ((uint64_t)T << 16) | ((uint64_t)n << 32);
+        }
+      }
+#endif
     } else {
       // radix-select among all candidates (same marks in every CTA), then each CTA
       // emits its own marked candidates at their position among the marked ones
@@ -1410,6 +1439,10 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   if (fallback) {
     if (!refine_in_place(c, u, b0, need, above0, fa, fo, le0)) return;
   }
+  // The row histogram bins this CTA published are read by every CTA of the row before
+  // its barrier-2 arrival; clear them for the next call (off the critical path).
+  if (overlap)
+    for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
   TOPK_MARK(g_select_trace, 8);
 }
 
@@ -1427,6 +1460,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     const int4 h1 = *reinterpret_cast<const int4*>(reinterpret_cast<const char*>(h) + 16);
     const int4 h2 = *reinterpret_cast<const int4*>(reinterpret_cast<const char*>(h) + 32);
     s.ud = units[blockIdx.x];
+    s.bc[29] = reinterpret_cast<const int32_t*>(p.ws + lay.first_single)[blockIdx.x];
     s.bc[20] = h0.x;  // magic
     s.bc[21] = h0.y;  // rows
     s.bc[22] = h0.z;  // max_len
@@ -1492,10 +1526,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   }
 
   const int2* singles = reinterpret_cast<const int2*>(p.ws + lay.singles);
-  const int32_t* first_single = reinterpret_cast<const int32_t*>(p.ws + lay.first_single);
-  int idx = first_single[blockIdx.x];
+  // The single row the plan hands this CTA (read in the prologue), then tickets; when
+  // the plan hands out every single row, no CTA claims one (each call then advances
+  // the ticket counter by 0, a multiple of its period, as the modular claims need).
+  int idx = s.bc[29];
   bool implicit = idx >= 0;
+  const bool tickets = n_single > n_implicit;
   while (true) {
+    if (!implicit && !tickets) break;
     if (!implicit) {
       __syncthreads();
       if (threadIdx.x == 0) {
