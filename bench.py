@@ -196,6 +196,24 @@ class _Flush:
         torch.sum(self.r, dim=0, out=self.acc)
 
 
+def max_over_ranks(x: float, n: int, device) -> float:
+    """The largest of every rank's x (the whole job lasts as long as its slowest
+    rank); x itself when there is one rank."""
+    if n <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(n: int, score_bytes: int, steps: int, total_ms: float) -> float:
+    """Score GB/s of the whole job: n replicas each processing `steps` batches of
+    `score_bytes`, in the slowest rank's `total_ms`."""
+    return n * score_bytes * steps / (total_ms / 1e3) / 1e9
+
+
 def _time(fn, steps, flush):
     """Per-step CUDA-event times (ms) of fn(), L2 flushed before each (outside the events)."""
     import torch
@@ -314,14 +332,9 @@ def run_ours(args):
     if n > 1:
         torch.distributed.barrier()
 
-    total_ms = float(sum(step_ms))
-    if n > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(float(sum(step_ms)), n, dev)
     score_bytes = 4 * int(b1m.lens.astype(np.int64).sum())
-    value = n * score_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = job_throughput_gbs(n, score_bytes, args.steps, total_ms)
     ms_step = total_ms / args.steps
     nsec = min(args.steps, 300)
     sel_ms = _time(bt.g_select.replay, nsec, flush)
