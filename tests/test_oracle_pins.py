@@ -133,7 +133,7 @@ def pin_closed_forms(mutant=0):
 
 
 def pin_invariants(mutant=0, big=False):
-    batches = [W.pr1(), W.mixed_decode()]
+    batches = [W.pr1(), W.mixed_decode(), W.prefill(prefixes=(2048, 5000), q=(512, 300))]
     adv = W.adversarial()
     batches += [adv]
     if big:
@@ -196,7 +196,8 @@ def test_oracle_invariants_long_rows():
 
 
 def test_nth_element_cross_check():
-    for b in [W.pr1(), W.mixed_decode(), W.adversarial()] + W.tiny_rows():
+    for b in ([W.pr1(), W.mixed_decode(), W.adversarial(),
+               W.prefill(prefixes=(2048, 5000), q=(512, 300))] + W.tiny_rows()):
         for k in (b.ks or [b.k]):
             s1, p1, e1 = oracle.topk_batch(b, k=k, threads=4)
             s2, p2, e2 = oracle.topk_batch(b, k=k, threads=4, use_nth=True)

@@ -59,6 +59,20 @@ def test_verify_1m():
     compare_with_oracle(b, b.k, slots, pos)
 
 
+def test_prefill_ragged():
+    """Ragged prefill: two requests (prefix 2048 and 5000 tokens, 512 and 300 new
+    queries), causal row lengths stepping by one, rows mapped to their request's table;
+    every k class."""
+    b = W.prefill(prefixes=(2048, 5000), q=(512, 300))
+    dev = to_dev(b)
+    core = PagedTopK(b.rows, b.max_len)
+    core.plan(dev[1])
+    for k in (1, 100, 2048):
+        slots, pos, st = run_gpu(b, k=k, plan=core, dev_inputs=dev)
+        assert st == 0
+        compare_with_oracle(b, k, slots, pos)
+
+
 def test_mixed_decode():
     b = W.mixed_decode()
     slots, pos, st = run_gpu(b)

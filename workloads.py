@@ -224,12 +224,35 @@ def adversarial(seed: int = SEED_BASE + 4, rows: int = 256, max_len: int = 32768
     return Batch("adversarial", s, lens, max_len, ks[0], tab, None, ps, ks=ks)
 
 
+def prefill(seed: int = SEED_BASE + 5, prefixes=(8192,), q=(4096,), k: int = 2048,
+            page_size: int = 64) -> Batch:
+    """Ragged prefill: request j has prefixes[j] cached tokens and q[j] new query tokens;
+    query i of request j scores the causal prefix of length prefixes[j] + i + 1. Rows
+    are the queries of all requests in order (thousands of rows whose lengths step by
+    one); scores N(0,1); each request's pages come from one shuffled pool and every
+    row maps to its request's table (row_to_table)."""
+    rng = _rng(seed)
+    lens, r2t = [], []
+    for j, (pre, nq) in enumerate(zip(prefixes, q)):
+        lens.extend(pre + i + 1 for i in range(nq))
+        r2t.extend([j] * nq)
+    lens = np.array(lens, dtype=np.int32)
+    max_len = int(max(p + n for p, n in zip(prefixes, q)))
+    s = _empty_scores(len(lens), round_up(max_len, 4))
+    for r, l in enumerate(lens):
+        s[r, :l] = rng.standard_normal(int(l)).astype(np.float32)
+    req_len = np.array([p + n for p, n in zip(prefixes, q)], dtype=np.int32)
+    tab = _tables_from_pool(rng, req_len, page_size, -(-max_len // page_size))
+    return Batch("prefill", s, lens, max_len, k, tab, np.array(r2t, dtype=np.int32), page_size)
+
+
 CONFIGS = {
     "pr1_ref": pr1,
     "verify_80k": verify_80k,
     "verify_1m": verify_1m,
     "mixed_decode": mixed_decode,
     "adversarial": adversarial,
+    "prefill": prefill,
 }
 
 
