@@ -31,17 +31,21 @@ namespace {
 #ifdef TOPK_TRACE
 __device__ uint64_t g_select_trace[kMaxGrid * 32];
 // Per-CTA event log: (row + 1) << 44 | event << 40 | low 40 bits of %globaltimer.
-__device__ uint64_t g_select_log[kMaxGrid * 64];
+__device__ uint64_t g_select_log[kMaxGrid * 256];
 __device__ int g_select_log_n[kMaxGrid];
+__device__ __forceinline__ int& trace_log_n() {
+  __shared__ int n;  // events logged by this CTA (written out at the end)
+  return n;
+}
 #define TOPK_LOG(row, ev)                                                              \
   do {                                                                                 \
     if (threadIdx.x == 0) {                                                            \
-      const int n_ = g_select_log_n[blockIdx.x];                                       \
-      if (n_ < 64)                                                                     \
-        g_select_log[blockIdx.x * 64 + n_] = ((uint64_t)((row) + 1) << 44) |           \
-                                             ((uint64_t)(ev) << 40) |                  \
-                                             (global_timer_ns() & 0xFFFFFFFFFFull);    \
-      g_select_log_n[blockIdx.x] = n_ + 1;                                             \
+      const int n_ = trace_log_n();                                                    \
+      if (n_ < 256)                                                                    \
+        g_select_log[blockIdx.x * 256 + n_] = ((uint64_t)((row) + 1) << 44) |          \
+                                              ((uint64_t)(ev) << 40) |                 \
+                                              (global_timer_ns() & 0xFFFFFFFFFFull);   \
+      trace_log_n() = n_ + 1;                                                          \
     }                                                                                  \
   } while (0)
 #else
@@ -1050,65 +1054,78 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   __syncthreads();  // histogram region is free: reused for the staging lists
   TOPK_MARK(g_select_trace, 17);
 
-  // Pass 2 over the resident chunk: a float filter skips vectors below the threshold
-  // bin. First each
-  // thread counts the values it will stage (positions above the threshold bin,
-  // boundary candidates) or folds the boundary keys (fallback) and remembers up to
-  // two vectors that held any; a CTA scan turns the counts into offsets; then those
-  // threads write them (rescanning only when they saw more). No shared atomics; the
-  // staging order is deterministic. For a threshold bin on the positive side the
-  // bin's float bounds are exact, so values are classified by two compares.
+  // Pass 2 over the resident chunk, in two steps with a CTA scan between them. Count:
+  // each thread reads its vectors (v = threadIdx.x + i * kThreads), skips those whose
+  // largest value lies below the threshold bin (nearly all of a long row), counts the
+  // values it will stage (positions above the threshold bin, boundary candidates) or
+  // folds the boundary keys (fallback), and sets bit i of a mask for each vector that
+  // held a value to stage. Write: after the scan turns the counts into offsets, each
+  // thread revisits only its masked vectors. No shared atomics; the staging order is
+  // deterministic. For a threshold bin on the positive side the bin's float bounds
+  // are exact, so values are classified by compares alone and each vector's values go
+  // to their slots by popcounts of its compare masks, without branches.
+  static_assert((kBufFloats / 4 + kThreads - 1) / kThreads <= 32,
+                "a thread's vectors of one chunk fit the 32-bit hit mask");
   const float tlo = skip_below((uint32_t)b0);
   const bool exact = b0 >= 2048 && b0 < 4095 && !fallback;
   const float thi = exact ? skip_below((uint32_t)b0 + 1u) : 0.0f;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   uint32_t fa = 0xFFFFFFFFu, fo = 0u;
-  int na = 0, nc = 0, nhv = 0;
-  // Vectors holding values to stage, newest first, 16 bits each (nvec < 2^16) in two
-  // words; the write step below revisits them when a thread has at most eight (a
-  // thread holds 0.8 such vectors on average on the 1M rows; more than eight would
-  // make it rescan the chunk while the CTA waits).
-  unsigned long long hvs = 0ull, hvs2 = 0ull;
-  // classify one value: 0 below, 1 above (staged position), 2 boundary candidate
+  int na = 0, nc = 0;
+  uint32_t hm = 0u;  // bit i: this thread's i-th vector holds a value to stage
+  // The chunk's first and last vectors may hold values of the neighbouring chunks:
+  // those become -inf, below tlo (exact mode has tlo >= +0).
+  const int vfull0 = (u.head + 3) >> 2, vfull1 = (u.head + u.n) >> 2;
+  auto clip = [&](int v, float4& x) {
+    if (v < vfull0 || v >= vfull1) {
+      const int e0 = 4 * v - u.head;
+      const float ninf = __int_as_float(0xFF800000);
+      if (e0 < 0 || e0 >= u.n) x.x = ninf;
+      if (e0 + 1 < 0 || e0 + 1 >= u.n) x.y = ninf;
+      if (e0 + 2 < 0 || e0 + 2 >= u.n) x.z = ninf;
+      if (e0 + 3 < 0 || e0 + 3 >= u.n) x.w = ninf;
+    }
+  };
+  // bit j set iff component j of x is >= t
+  auto ge_mask = [](const float4& x, float t) -> uint32_t {
+    return (x.x >= t ? 1u : 0u) | (x.y >= t ? 2u : 0u) | (x.z >= t ? 4u : 0u) |
+           (x.w >= t ? 8u : 0u);
+  };
+  // classify one value (non-exact mode): 0 below, 1 above (staged position), 2 boundary
   auto klass = [&](float x) -> int {
-    if (exact) return x >= tlo ? ((x >= thi || all_eq) ? 1 : 2) : 0;
     const uint32_t dg = coarse_digit(x);
     if (dg < (uint32_t)b0) return 0;
     return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
   };
-  auto ge4 = [](const float4& x, float t) {
-    return (x.x >= t) + (x.y >= t) + (x.z >= t) + (x.w >= t);
-  };
   if (exact) {
-    // Branch-free over every vector (shared-memory bound): exact counts from two
-    // compares per value. The chunk's first and last vectors mask the values outside
-    // it (to -inf, below tlo >= 0).
-    const int vfull0 = (u.head + 3) >> 2, vfull1 = (u.head + u.n) >> 2;
-    for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-      float4 x = b4[v];
-      if (v < vfull0 || v >= vfull1) {
-        const int e0 = 4 * v - u.head;
-        const float ninf = __int_as_float(0xFF800000);
-        if (e0 < 0 || e0 >= u.n) x.x = ninf;
-        if (e0 + 1 < 0 || e0 + 1 >= u.n) x.y = ninf;
-        if (e0 + 2 < 0 || e0 + 2 >= u.n) x.z = ninf;
-        if (e0 + 3 < 0 || e0 + 3 >= u.n) x.w = ninf;
+    auto count = [&](int i, int v, float4 x) {
+      clip(v, x);
+      const uint32_t mg = ge_mask(x, tlo);
+      const uint32_t ma = all_eq ? mg : ge_mask(x, thi);
+      const uint32_t mc = stage_cand ? (mg & ~ma) : 0u;
+      na += __popc(ma);
+      nc += __popc(mc);
+      hm |= (ma | mc) ? (1u << i) : 0u;
+    };
+    // This CTA holds la0 + le0 values at or above the threshold bin. Sparse (under
+    // one per 16 vectors, the usual case on long rows): most warps' vectors are all
+    // below tlo, so a max filter skips them. Dense: every warp would take the branch,
+    // so every vector is classified without one.
+    if ((int64_t)(la0 + le0) * 16 < u.nvec) {
+      for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) {
+        const float4 x = b4[v];
+        if (vmax4(x) >= tlo) count(i, v, x);
       }
-      const int g = ge4(x, tlo);
-      const int a = all_eq ? g : ge4(x, thi);
-      na += a;
-      nc += g - a;
-      const bool h = g > 0;
-      hvs2 = h ? ((hvs2 << 16) | (hvs >> 48)) : hvs2;
-      hvs = h ? ((hvs << 16) | (unsigned long long)v) : hvs;
-      nhv += h ? 1 : 0;
+    } else {
+      for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) count(i, v, b4[v]);
     }
-    if (!stage_cand) nc = 0;
   } else {
-    auto count = [&](int v, const float4& x) {
+    for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) {
+      const float4 x = b4[v];
+      if (vmax4(x) < tlo) continue;
       const int e0 = 4 * v - u.head;
-      int a = 0, cd = 0;
       const float xs[4] = {x.x, x.y, x.z, x.w};
+      int a = 0, cd = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int e = e0 + j;
@@ -1126,20 +1143,13 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         }
       }
       if (!stage_cand) cd = 0;
-      if (a + cd) {
-        na += a;
-        nc += cd;
-        hvs2 = (hvs2 << 16) | (hvs >> 48);
-        hvs = (hvs << 16) | (unsigned long long)v;
-        ++nhv;
-      }
-    };
-    for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-      const float4 x0 = b4[v];
-      if (!(vmax4(x0) < tlo)) count(v, x0);
+      na += a;
+      nc += cd;
+      hm |= (a + cd) ? (1u << i) : 0u;
     }
   }
-#ifdef TOPK_TRACE
+  TOPK_LOG(u.r, 6);
+#ifdef TOPK_TRACE_DETAIL  // block-wide timing; distorts the phases it brackets
   if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 18] = global_timer_ns();
   {
     // slowest thread of the count pass
@@ -1149,7 +1159,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     atomicMax(&tmax, (unsigned long long)global_timer_ns());
     __syncthreads();
     if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 20] = tmax;
-    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 21] = nhv;
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 21] = __popc(hm);
   }
 #endif
   int tot_ac;
@@ -1158,13 +1168,37 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     s.bc[9] = tot_ac & 0xFFFF;  // staged emissions
     s.bc[10] = tot_ac >> 16;    // staged candidates
   }
+  TOPK_LOG(u.r, 7);
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 19] = global_timer_ns();
 #endif
-  if (na + nc > 0) {
-    int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
-    auto write = [&](int v) {
-      const float4 x = b4[v];
+  int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
+  while (hm) {
+    const int i = __ffs(hm) - 1;
+    hm &= hm - 1u;
+    const int v = threadIdx.x + i * kThreads;
+    float4 x = b4[v];
+    const int p0 = u.s0 + 4 * v - u.head;  // position of component 0
+    if (exact) {
+      clip(v, x);
+      const uint32_t mg = ge_mask(x, tlo);
+      const uint32_t ma = all_eq ? mg : ge_mask(x, thi);
+      const uint32_t mc = stage_cand ? (mg & ~ma) : 0u;
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t below = (1u << j) - 1u;
+        const int o = oa + __popc(ma & below);
+        if (((ma >> j) & 1u) && o < TOPK_MAX_K) s.u.l.elist[o] = p0 + j;
+        const int q = oc + __popc(mc & below);
+        if (((mc >> j) & 1u) && q < kListCap) {
+          s.u.l.ckey[q] = f2key(xs[j]);
+          s.u.l.cpos[q] = (uint32_t)(p0 + j);
+        }
+      }
+      oa += __popc(ma);
+      oc += __popc(mc);
+    } else {
       const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -1172,29 +1206,19 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         if (e < 0 || e >= u.n) continue;
         const int k = klass(xs[j]);
         if (k == 1) {
-          if (oa < TOPK_MAX_K) s.u.l.elist[oa] = u.s0 + e;
+          if (oa < TOPK_MAX_K) s.u.l.elist[oa] = p0 + j;
           ++oa;
         } else if (k == 2 && stage_cand) {
           if (oc < kListCap) {
             s.u.l.ckey[oc] = f2key(xs[j]);
-            s.u.l.cpos[oc] = (uint32_t)(u.s0 + e);
+            s.u.l.cpos[oc] = (uint32_t)(p0 + j);
           }
           ++oc;
         }
       }
-    };
-    if (nhv <= 8) {
-      for (int i = 0; i < nhv; ++i)
-        write((int)(((i < 4 ? hvs : hvs2) >> (16 * (i & 3))) & 0xFFFFu));
-    } else {
-      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-        const float4 x = b4[v];
-        if (fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) < tlo) continue;
-        write(v);
-      }
     }
   }
-#ifdef TOPK_TRACE
+#ifdef TOPK_TRACE_DETAIL  // block-wide timing; distorts the phases it brackets
   {
     __shared__ unsigned long long wmax;
     if (threadIdx.x == 0) wmax = 0;
@@ -1207,6 +1231,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
 #endif
   __syncthreads();  // staging lists and counts complete
   TOPK_MARK(g_select_trace, 4);
+  TOPK_LOG(u.r, 4);
   if (fallback) block_and_or(fa, fo, s);
 
   // Multi-CTA rows: per-rank candidate slots let one barrier carry both the counts
@@ -1324,6 +1349,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     for (int i = threadIdx.x; i < n_emit; i += kThreads) emit(c, u, out_base + i, s.u.l.elist[i]);
   }
 
+  TOPK_LOG(u.r, 5);
   if (compact && u.G == 1) {
     __syncthreads();
     select_boundary(c, u, s.u.l.ckey, s.u.l.cpos, s.cst, min(eq0, kListCap), need, above0);
@@ -1402,7 +1428,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
           else emit(c, u, above0 + rank, (int)pi);
         }
       }
-#ifdef TOPK_TRACE
+#ifdef TOPK_TRACE_DETAIL  // block-wide timing; distorts the phases it brackets
       {
         const long long qe = clock64();
         __shared__ unsigned long long qmx;
@@ -1444,6 +1470,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   if (overlap)
     for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
   TOPK_MARK(g_select_trace, 8);
+  TOPK_LOG(u.r, 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
@@ -1505,7 +1532,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   const int waves = s.bc[24], n_single = s.bc[25], n_implicit = s.bc[27];
   const int dyn_period = s.bc[28];
 #ifdef TOPK_TRACE
-  if (threadIdx.x == 0) g_select_log_n[blockIdx.x] = 0;
+  if (threadIdx.x == 0) trace_log_n() = 0;
   TOPK_LOG(-1, 0);
 #endif
 
@@ -1558,13 +1585,16 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     process_unit(c, d, false);
   }
   TOPK_MARK(g_select_trace, 9);
+#ifdef TOPK_TRACE
+  if (threadIdx.x == 0) g_select_log_n[blockIdx.x] = trace_log_n();
+#endif
 }
 
 }  // namespace
 
 #ifdef TOPK_TRACE
 extern "C" int topk_trace_log(uint64_t* host, int* counts) {
-  if (cudaMemcpyFromSymbol(host, g_select_log, sizeof(uint64_t) * kMaxGrid * 64) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(host, g_select_log, sizeof(uint64_t) * kMaxGrid * 256) != cudaSuccess)
     return -9;
   return cudaMemcpyFromSymbol(counts, g_select_log_n, sizeof(int) * kMaxGrid) == cudaSuccess ? 0 : -9;
 }
