@@ -633,6 +633,7 @@ __device__ void histogram_chunk(Ctx& c, Unit& u) {
   const int vfull1 = (u.head + u.n) >> 2;
   for (int p = 0; p < u.npieces; ++p) {
     wait_piece(c, p);
+    if (p == u.npieces - 1) TOPK_LOG(u.r, 10);
     if (threadIdx.x == 0 && p + kWindow < u.npieces) issue_copies(s, u.src, u.bytes, p + kWindow, 1);
     const int vend = min((p + 1) * kVecPerPiece, u.nvec);
     for (int v = p * kVecPerPiece + threadIdx.x; v < vend; v += kThreads) {
@@ -1030,6 +1031,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   }
 
   __syncthreads();  // histogram zeroed
+  TOPK_LOG(u.r, 9);
   histogram_chunk(c, u);
   TOPK_MARK(g_select_trace, 2);
   TOPK_LOG(u.r, 2);
