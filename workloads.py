@@ -263,3 +263,92 @@ def with_ld(b: Batch, ld: int) -> Batch:
     w = min(ld, b.ld)
     s[:, :w] = b.scores[:, :w]
     return dataclasses.replace(b, scores=s)
+
+
+# ---------------------------------------------------------------- key-path prologue
+@dataclasses.dataclass
+class KeyBatch:
+    """Inputs of one call of the indexer key-path prologue (LayerNorm, RoPE, FP8 store
+    into the paged indexer KV cache) for T tokens of D channels."""
+
+    name: str
+    k_bf16: np.ndarray        # uint16 [T, D]: bfloat16 bit patterns (the wk projection's output)
+    ln_w: np.ndarray          # float32 [D]
+    ln_b: np.ndarray          # float32 [D]
+    eps: float
+    positions: np.ndarray     # int32 [T]: logical position of each token in its request
+    cos_sin: np.ndarray       # float32 [max_pos, R]: cos of the R / 2 pair angles, then sines
+    rope_dim: int
+    token_table: np.ndarray   # int32 [T]: block-table row of each token's request
+    block_table: np.ndarray   # int32 [n_req, table_ld]
+    page_size: int
+    num_slots: int
+
+    @property
+    def tokens(self) -> int:
+        return int(self.k_bf16.shape[0])
+
+    @property
+    def dim(self) -> int:
+        return int(self.k_bf16.shape[1])
+
+    def algorithmic_bytes(self) -> int:
+        """Keys, positions, token tables and each token's cos/sin row read once (the
+        distinct positions' rows), each used table entry once; codes and scales
+        written once."""
+        T, D = self.k_bf16.shape
+        rows = len(np.unique(self.positions[(self.positions >= 0) &
+                                            (self.positions < self.cos_sin.shape[0])]))
+        pages = len(np.unique(self.token_table.astype(np.int64) * (1 << 32) +
+                              self.positions.astype(np.int64) // self.page_size))
+        return T * (2 * D + 8) + rows * 4 * self.rope_dim + 4 * pages + T * (D + 4)
+
+
+def rope_table(max_pos: int, rope_dim: int, base: float = 10000.0) -> np.ndarray:
+    """cos / sin of the angles p * base^(-2i / R), p < max_pos, i < R / 2, as float32
+    [max_pos, R] (cosines first): the caller-side table a RoPE kernel reads."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    inv = base ** (-2.0 * i / rope_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def _to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even) and return the bits."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def key_prologue(seed: int = SEED_BASE + 6, reqs=((0, 16384), (4000, 4096), (100000, 7)),
+                 dim: int = 128, rope_dim: int = 64, page_size: int = 64,
+                 max_pos: int = 131072) -> KeyBatch:
+    """Tokens of several requests in one call: request j contributes n_j tokens at
+    positions start_j, ..., start_j + n_j - 1 (a prefill chunk, or a few decode
+    tokens). Key channels are N(0,1) times a per-channel spread (exp of N(0, 0.5)) plus
+    a per-channel offset N(0, 0.5), rounded to bfloat16; LayerNorm weight 1 + N(0, 0.1),
+    bias N(0, 0.1), eps 1e-6; RoPE base 10000. Each request's pages are drawn from one
+    shuffled pool of physical pages; the cache has exactly the pool's slots."""
+    rng = _rng(seed)
+    spread = np.exp(rng.normal(0.0, 0.5, dim))
+    offset = rng.normal(0.0, 0.5, dim)
+    pos, t2t = [], []
+    for j, (start, n) in enumerate(reqs):
+        pos.extend(range(start, start + n))
+        t2t.extend([j] * n)
+    T = len(pos)
+    x = (rng.standard_normal((T, dim)) * spread + offset).astype(np.float32)
+    ends = np.array([s + n for s, n in reqs], dtype=np.int64)
+    table_ld = int(-(-int(ends.max()) // page_size))
+    need = [int(-(-e // page_size)) for e in ends]
+    pool = _shuffled_pages(rng, sum(need))
+    tab = np.full((len(reqs), table_ld), -1, np.int32)
+    at = 0
+    for j, m in enumerate(need):
+        tab[j, :m] = pool[at:at + m]
+        at += m
+    return KeyBatch("key_prologue", _to_bf16_bits(x),
+                    (1.0 + rng.normal(0.0, 0.1, dim)).astype(np.float32),
+                    rng.normal(0.0, 0.1, dim).astype(np.float32), 1e-6,
+                    np.array(pos, np.int32), rope_table(max_pos, rope_dim), rope_dim,
+                    np.array(t2t, np.int32), tab, page_size, int(sum(need)) * page_size)
