@@ -24,9 +24,10 @@ also listed in the design doc):
 * The token at logical position p of request r is stored at the physical slot
   table[r][p / page_size] * page_size + p % page_size, the slot rule of the top-k
   path's page translation; codes go to cache[slot, 0:D], the scale to scale[slot].
-* A token whose position lies outside the cos/sin table or the table row, whose page
-  entry is negative, or whose slot lies outside the cache is not stored, and sets a
-  status bit (the same bits as the kernel's).
+* A token whose position lies outside the cos/sin table or the table row, whose
+  block-table row does not exist, whose page entry is negative, or whose slot lies
+  outside the cache is not stored, and sets a status bit (the same bits as the
+  kernel's), checked in that order.
 
 Arithmetic is fp64 up to y / scale; the rounding to e4m3 is exact from that value.
 """
@@ -40,6 +41,7 @@ ERR_POSITION = 1    # position < 0 or >= the cos/sin table's rows
 ERR_TABLE_WIDTH = 2  # position / page_size >= table_ld
 ERR_TABLE_ENTRY = 4  # negative page entry
 ERR_SLOT = 8        # slot outside [0, num_slots)
+ERR_TABLE_ROW = 16  # token's block-table row outside [0, n_tables)
 
 # Deliberately wrong variants, for the pin-strength test (0 = the oracle).
 MUTANTS = {
@@ -160,6 +162,9 @@ def slots_of(positions, token_table, block_table, page_size, num_slots, mutant=0
     for i, (p, t) in enumerate(zip(pos, t2t)):
         if p < 0:
             err |= ERR_POSITION
+            continue
+        if t < 0 or t >= tab.shape[0]:
+            err |= ERR_TABLE_ROW
             continue
         pg, off = (p % ps, p // ps) if mutant == 6 else (p // ps, p % ps)
         if pg >= tab.shape[1]:

@@ -32,7 +32,7 @@ EXPORTS = (
     "topk_workspace_bytes", "topk_max_row_len", "topk_chunk_capacity", "topk_plan",
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
-    "topk_select_paged_noalloc",
+    "topk_select_paged_noalloc", "indexer_k_prologue",
 )
 
 
@@ -62,7 +62,28 @@ _SIGS = {
     "topk_layout_info": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int64), _c.c_int]),
     "topk_select_paged_noalloc": (_c.c_int, [_VP, _c.c_int64, _VP, _c.c_int, _c.c_int, _c.c_int,
                                              _VP, _c.c_int64, _VP, _c.c_int, _VP, _VP, _VP, _VP]),
+    "indexer_k_prologue": (_c.c_int, [_VP, _c.c_int64, _c.c_int, _c.c_int, _VP, _VP, _c.c_float,
+                                      _VP, _VP, _c.c_int, _c.c_int, _VP, _VP, _c.c_int,
+                                      _c.c_int64, _c.c_int, _VP, _VP, _c.c_int64, _VP, _VP]),
 }
+
+# include/indexer_prologue.h
+PROLOGUE_OK = 0
+PROLOGUE_ERR_NULL = -1
+PROLOGUE_ERR_SHAPE = -2
+PROLOGUE_ERR_ALIGN = -3
+PROLOGUE_ERR_CUDA = -4
+PROLOGUE_STATUS_POSITION = 1
+PROLOGUE_STATUS_TABLE_WIDTH = 2
+PROLOGUE_STATUS_TABLE_ENTRY = 4
+PROLOGUE_STATUS_SLOT = 8
+PROLOGUE_STATUS_TABLE_ROW = 16
+
+
+class PrologueError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"indexer_k_prologue: {code}")
+        self.code = code
 
 
 def lib():
@@ -178,6 +199,26 @@ def topk_plan_host(lens, rows: int, max_len: int, grid: int, chunk: int, image) 
                                        int(max_len), int(grid), int(chunk),
                                        image.ctypes.data_as(ctypes.c_void_p), int(image.nbytes)),
                   "topk_plan_host")
+
+
+def indexer_k_prologue(k, ln_w, ln_b, eps: float, positions, cos_sin, rope_dim: int,
+                       token_table, block_table, page_size: int, cache, cache_scale,
+                       status=None, stream=None) -> int:
+    """indexer_k_prologue of include/indexer_prologue.h on CUDA tensors: k (bf16 or
+    its int16 bits) [tokens, ld], ln_w / ln_b float32 [dim], positions / token_table
+    int32 [tokens], cos_sin float32 [max_pos, rope_dim], block_table int32
+    [n_tables, table_ld], cache uint8 [num_slots, dim], cache_scale float32
+    [num_slots], status int32 [1] or None. Argument marshalling only."""
+    tokens, ld = (int(k.shape[0]), int(k.stride(0))) if k.dim() == 2 else (0, 0)
+    dim = int(k.shape[1]) if k.dim() == 2 else 0
+    code = lib().indexer_k_prologue(
+        _ptr(k), ld, tokens, dim, _ptr(ln_w), _ptr(ln_b), float(eps), _ptr(positions),
+        _ptr(cos_sin), int(cos_sin.shape[0]), int(rope_dim), _ptr(token_table),
+        _ptr(block_table), int(block_table.shape[0]), int(block_table.stride(0)), int(page_size),
+        _ptr(cache), _ptr(cache_scale), int(cache.shape[0]), _ptr(status), _stream(stream))
+    if code < 0:
+        raise PrologueError(code)
+    return code
 
 
 def topk_layout_info(rows: int):

@@ -1,7 +1,8 @@
 """Builds the CUDA library libtopk_paged.so in-tree for sm_103a with nvcc.
 
-Four translation units are compiled in parallel and linked into one shared library
-that exports the C ABI of include/topk_paged.h (no torch types cross it).
+Five translation units are compiled in parallel and linked into one shared library
+that exports the C ABI of include/topk_paged.h and include/indexer_prologue.h (no
+torch types cross it).
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
-SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu"]
+SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu"]
 HEADERS = ["common.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -48,7 +49,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     lib = LIB.replace(".so", "_trace.so") if trace else LIB
     defs = ["-DTOPK_TRACE"] if trace else []
     os.makedirs(bdir, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "topk_paged.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", h)
+                                                        for h in ("topk_paged.h", "indexer_prologue.h")]
     objs = []
     jobs = []
     for src in SOURCES:

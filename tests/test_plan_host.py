@@ -27,17 +27,21 @@ def _lib_or_skip():
 
 
 def header_exports():
-    src = open(os.path.join(ROOT, "include", "topk_paged.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(topk_[a-z_]+)\s*\(", src)))
+    names = set()
+    for h in ("topk_paged.h", "indexer_prologue.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b((?:topk|indexer)_[a-z_]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported():
     lib = _lib_or_skip()
     names = header_exports()
     assert "topk_select_paged" in names and "topk_plan" in names
+    assert "indexer_k_prologue" in names
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in include/topk_paged.h but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
     assert set(names) <= set(B.EXPORTS), set(names) - set(B.EXPORTS)
 
 
