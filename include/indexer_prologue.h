@@ -38,9 +38,9 @@ enum {
   INDEXER_ERR_SHAPE = -2,  /* tokens < 0, dim != 128, rope_dim odd or outside [0, dim],
                               max_pos < 1, page_size < 1, n_tables < 1, table_ld < 1,
                               num_slots < 0,
-                              ld < dim or ld not a multiple of 4, eps negative or not finite */
-  INDEXER_ERR_ALIGN = -3,  /* k not 8-byte aligned, ln_w / ln_b not 16-byte aligned,
-                              cache, cos_sin or the int32 arrays not 4-byte aligned */
+                              ld < dim or ld not a multiple of 8, eps negative or not finite */
+  INDEXER_ERR_ALIGN = -3,  /* k, ln_w or ln_b not 16-byte aligned, cache not 8-byte
+                              aligned, cos_sin or the int32 arrays not 4-byte aligned */
   INDEXER_ERR_CUDA = -4    /* the launch failed */
 };
 
@@ -55,8 +55,8 @@ enum {
 
 /* One launch on `stream`; every argument error is reported before anything is
  * enqueued.
- *   k           device bf16 bits (uint16) [tokens, ld], row-major; 8-byte aligned,
- *               ld a multiple of 4; channels [0, dim) of each row are read
+ *   k           device bf16 bits (uint16) [tokens, ld], row-major; 16-byte aligned,
+ *               ld a multiple of 8; channels [0, dim) of each row are read
  *   tokens      number of tokens (rows of k); 0 enqueues nothing
  *   dim         channels per token: 128 (the indexer head dimension)
  *   ln_w, ln_b  device float32 [dim], 16-byte aligned: LayerNorm weight and bias
@@ -70,7 +70,7 @@ enum {
  *   block_table device int32 [n_tables, table_ld]: physical page ids (< 0: no page)
  *   n_tables    rows of block_table (>= 1)
  *   page_size   tokens per page (>= 1)
- *   cache       device uint8 [num_slots, dim], 4-byte aligned: e4m3 codes (written)
+ *   cache       device uint8 [num_slots, dim], 8-byte aligned: e4m3 codes (written)
  *   cache_scale device float32 [num_slots]: per-token scales (written)
  *   status      device int32 [1] or NULL: INDEXER_STATUS_* bits are OR-ed in (the
  *               caller clears it); slots of tokens with a status bit are not touched

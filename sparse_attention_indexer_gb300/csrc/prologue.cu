@@ -3,13 +3,14 @@
 // Prologue Fusion", Figure 5). The readings of the steps' parameters are stated in
 // include/indexer_prologue.h.
 //
-// HBM-bound elementwise work with three per-token reductions: one warp per token,
-// lane l holding channels [4l, 4l + 4) of the 128. The key row is one coalesced
-// 256-byte load (8 bytes per lane), the codes one coalesced 128-byte store (4 bytes
-// per lane); LayerNorm's mean and variance and the absolute maximum are warp
-// shuffles; RoPE's adjacent pairs (4l, 4l + 1) and (4l + 2, 4l + 3) sit inside one
-// lane, so the rotation needs no exchange. The position, the block-table entry and
-// the cos/sin row are loaded once per token and broadcast by the memory system.
+// HBM-bound elementwise work with three per-token reductions. The key row of a token
+// is one coalesced 256-byte load (16 bytes per lane of a half-warp) and its codes one
+// coalesced 128-byte store; LayerNorm's mean and variance and the absolute maximum
+// are shuffles inside the half-warp; RoPE's adjacent pairs sit inside one lane, so the
+// rotation needs no exchange. The scale's reciprocal (one division per token) and
+// rsqrtf keep the per-token instruction count low: the kernel is otherwise bound by
+// instruction issue, not by memory. They move y / scale by a few fp32 ulps, far
+// inside the tolerance a rounding-midpoint decision allows.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -40,27 +41,28 @@ struct Params {
   int n_tables;
   int64_t table_ld;
   int page_size;
+  int page_shift;  // log2(page_size) when it is a power of two, else -1
   uint8_t* cache;
   float* cache_scale;
   int64_t num_slots;
   int32_t* status;
 };
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sums / maxima over the 16 lanes of a half-warp (one token each half).
+__device__ __forceinline__ float half_sum(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
+__device__ __forceinline__ float half_max(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 8; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
-  return __uint_as_float(bits16 << 16);
-}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // (a, b) -> (a cos - b sin, a sin + b cos)
 __device__ __forceinline__ void rotate(float& a, float& b, float c, float s) {
@@ -70,86 +72,129 @@ __device__ __forceinline__ void rotate(float& a, float& b, float c, float s) {
   b = y;
 }
 
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Each half-warp takes one token at a time, lane h (0..15) holding channels
+// [8h, 8h + 8): the key row is one 16-byte load per lane, the codes one 8-byte store,
+// the three reductions four shuffle levels inside the half, and every scalar step
+// (slot, scale, reciprocal) serves two tokens per warp instruction. A warp takes
+// kTokensPerWarp consecutive tokens and issues all their loads before it waits on
+// any: the key rows with the positions and table rows, then (they depend on the
+// position) the page entries and cos/sin values.
+constexpr int kTokensPerWarp = 4;
+constexpr int kPairs = kTokensPerWarp / 2;
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) key_prologue_kernel(Params p) {
-  const int t = (int)(((int64_t)blockIdx.x * kWarpsPerBlock) + (threadIdx.x >> 5));
+  const int64_t w0 =
+      ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * kTokensPerWarp;
   const int lane = threadIdx.x & 31;
-  if (t >= p.tokens) return;  // whole warps leave together
+  const int h = lane & 15;       // lane within the half-warp
+  const int side = lane >> 4;    // which token of a pair
+  if (w0 >= p.tokens) return;    // whole warps leave together
 
-  // independent loads first: the key row, the token's position and table row, the
-  // LayerNorm parameters (L1/L2 resident across tokens)
-  const uint2 kv = __ldg(reinterpret_cast<const uint2*>(p.k + (int64_t)t * p.ld) + lane);
-  const int pos = __ldg(p.positions + t);
-  const int tab = __ldg(p.token_table + t);
-  const float4 w = __ldg(reinterpret_cast<const float4*>(p.ln_w) + lane);
-  const float4 bb = __ldg(reinterpret_cast<const float4*>(p.ln_b) + lane);
+  const float4* wv = reinterpret_cast<const float4*>(p.ln_w) + 2 * h;
+  const float4* bv = reinterpret_cast<const float4*>(p.ln_b) + 2 * h;
+  const float4 wa = __ldg(wv), wb = __ldg(wv + 1), ba = __ldg(bv), bb = __ldg(bv + 1);
+  uint4 kv[kPairs];
+  int pos[kPairs], tab[kPairs];
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    const int64_t t = w0 + 2 * j + side;
+    const bool in = t < p.tokens;
+    kv[j] = in ? __ldg(reinterpret_cast<const uint4*>(p.k + t * p.ld) + h) : make_uint4(0, 0, 0, 0);
+    pos[j] = in ? __ldg(p.positions + t) : -1;
+    tab[j] = in ? __ldg(p.token_table + t) : 0;
+  }
 
-  // the token's slot (warp-uniform decision)
+  // slots (uniform per half) and, for valid positions, this lane's cos/sin values:
+  // pairs 4h .. 4h + 3 cover channels 8h .. 8h + 7
+  const int half = p.rope_dim >> 1;
+  const int nrot = min(4, max(0, (p.rope_dim - 8 * h) >> 1));  // rotated pairs of this lane
+  int64_t slot[kPairs];
+  float cs[kPairs][4], sn[kPairs][4];
   int err = 0;
-  int64_t slot = -1;
-  if (pos < 0 || pos >= p.max_pos) {
-    err = INDEXER_STATUS_POSITION;
-  } else if (tab < 0 || tab >= p.n_tables) {
-    err = INDEXER_STATUS_TABLE_ROW;
-  } else {
-    const int pg = pos / p.page_size;
-    if ((int64_t)pg >= p.table_ld) {
-      err = INDEXER_STATUS_TABLE_WIDTH;
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    slot[j] = -1;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      cs[j][m] = 1.0f;
+      sn[j][m] = 0.0f;
+    }
+    if (w0 + 2 * j + side >= p.tokens) continue;
+    const int ps = pos[j];
+    if (ps < 0 || ps >= p.max_pos) {
+      err |= INDEXER_STATUS_POSITION;
+      continue;
+    }
+    if (tab[j] < 0 || tab[j] >= p.n_tables) {
+      err |= INDEXER_STATUS_TABLE_ROW;
     } else {
-      const int32_t page = __ldg(p.block_table + (int64_t)tab * p.table_ld + pg);
-      if (page < 0) {
-        err = INDEXER_STATUS_TABLE_ENTRY;
+      const int pg = p.page_shift >= 0 ? (ps >> p.page_shift) : ps / p.page_size;
+      if ((int64_t)pg >= p.table_ld) {
+        err |= INDEXER_STATUS_TABLE_WIDTH;
       } else {
-        slot = (int64_t)page * p.page_size + (pos - pg * p.page_size);
-        if (slot >= p.num_slots) err = INDEXER_STATUS_SLOT;
+        const int32_t page = __ldg(p.block_table + (int64_t)tab[j] * p.table_ld + pg);
+        const int64_t sl = (int64_t)page * p.page_size + (ps - pg * p.page_size);
+        if (page < 0) err |= INDEXER_STATUS_TABLE_ENTRY;
+        else if (sl >= p.num_slots) err |= INDEXER_STATUS_SLOT;
+        else slot[j] = sl;
       }
     }
+    const float* row = p.cos_sin + (int64_t)ps * p.rope_dim;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (m < nrot) {  // scalar loads: the sines start at rope_dim / 2, which may be odd
+        cs[j][m] = __ldg(row + 4 * h + m);
+        sn[j][m] = __ldg(row + half + 4 * h + m);
+      }
   }
-  if (err) {
-    if (lane == 0 && p.status) atomicOr(p.status, err);
-    return;
-  }
+  if (err && h == 0 && p.status) atomicOr(p.status, err);
 
-  // cos/sin of this lane's two pairs (pair i = 2l covers channels 4l, 4l + 1)
-  const int half = p.rope_dim >> 1;
-  float2 cs = make_float2(1.0f, 1.0f), sn = make_float2(0.0f, 0.0f);
-  const bool rot0 = 4 * lane < p.rope_dim, rot1 = 4 * lane + 2 < p.rope_dim;
-  if (rot0) {  // scalar loads: the sines start at rope_dim / 2, which may be odd
-    const float* row = p.cos_sin + (int64_t)pos * p.rope_dim;
-    cs.x = __ldg(row + 2 * lane);
-    sn.x = __ldg(row + half + 2 * lane);
-    if (rot1) {
-      cs.y = __ldg(row + 2 * lane + 1);
-      sn.y = __ldg(row + half + 2 * lane + 1);
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    // both halves run the shuffles; a half whose token is not stored skips the store
+    float x[8] = {bf16_lo(kv[j].x), bf16_hi(kv[j].x), bf16_lo(kv[j].y), bf16_hi(kv[j].y),
+                  bf16_lo(kv[j].z), bf16_hi(kv[j].z), bf16_lo(kv[j].w), bf16_hi(kv[j].w)};
+    // LayerNorm (two-pass mean / population variance over the 128 channels)
+    const float mean =
+        half_sum(((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]))) *
+        (1.0f / kDim);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i] -= mean;
+      ss = fmaf(x[i], x[i], ss);
     }
+    const float rstd = rsqrtf(half_sum(ss) * (1.0f / kDim) + p.eps);
+    const float wl[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    const float bl[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = fmaf(x[i] * rstd, wl[i], bl[i]);
+    // RoPE on the lane's pairs inside [0, rope_dim)
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (m < nrot) rotate(y[2 * m], y[2 * m + 1], cs[j][m], sn[j][m]);
+    // per-token scale and e4m3 codes (round to nearest even, saturate at +-448)
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(y[i]));
+    const float amax = half_max(a);
+    const float scale = amax > 0.0f ? amax / kE4m3Max : 1.0f;
+    const float inv = amax > 0.0f ? kE4m3Max / amax : 1.0f;
+    if (slot[j] < 0) continue;
+    const uint2 codes = make_uint2(e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
+                                   e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+    reinterpret_cast<uint2*>(p.cache + slot[j] * kDim)[h] = codes;
+    if (h == 0) p.cache_scale[slot[j]] = scale;
   }
-
-  // LayerNorm (two-pass mean / population variance over the 128 channels)
-  float x0 = bf16_bits_to_float(kv.x & 0xFFFFu), x1 = bf16_bits_to_float(kv.x >> 16);
-  float x2 = bf16_bits_to_float(kv.y & 0xFFFFu), x3 = bf16_bits_to_float(kv.y >> 16);
-  const float mean = warp_sum((x0 + x1) + (x2 + x3)) * (1.0f / kDim);
-  x0 -= mean;
-  x1 -= mean;
-  x2 -= mean;
-  x3 -= mean;
-  const float var = warp_sum((x0 * x0 + x1 * x1) + (x2 * x2 + x3 * x3)) * (1.0f / kDim);
-  const float rstd = 1.0f / sqrtf(var + p.eps);
-  float y0 = fmaf(x0 * rstd, w.x, bb.x), y1 = fmaf(x1 * rstd, w.y, bb.y);
-  float y2 = fmaf(x2 * rstd, w.z, bb.z), y3 = fmaf(x3 * rstd, w.w, bb.w);
-
-  // RoPE on the lane's pairs inside [0, rope_dim)
-  if (rot0) rotate(y0, y1, cs.x, sn.x);
-  if (rot1) rotate(y2, y3, cs.y, sn.y);
-
-  // per-token scale and e4m3 codes (round to nearest even, saturate at +-448)
-  const float amax = warp_max(fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3))));
-  const float scale = amax > 0.0f ? amax / kE4m3Max : 1.0f;
-  const __nv_fp8x2_storage_t lo =
-      __nv_cvt_float2_to_fp8x2(make_float2(y0 / scale, y1 / scale), __NV_SATFINITE, __NV_E4M3);
-  const __nv_fp8x2_storage_t hi =
-      __nv_cvt_float2_to_fp8x2(make_float2(y2 / scale, y3 / scale), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t codes = (uint32_t)lo | ((uint32_t)hi << 16);
-  reinterpret_cast<uint32_t*>(p.cache + slot * kDim)[lane] = codes;
-  if (lane == 0) p.cache_scale[slot] = scale;
 }
 
 bool aligned(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
@@ -165,20 +210,26 @@ extern "C" int indexer_k_prologue(const uint16_t* k, int64_t ld, int tokens, int
                                   int64_t num_slots, int32_t* status, indexer_stream_t stream) {
   if (tokens < 0 || dim != kDim || rope_dim < 0 || rope_dim > dim || (rope_dim & 1) ||
       max_pos < 1 || page_size < 1 || n_tables < 1 || table_ld < 1 || num_slots < 0 || ld < dim ||
-      (ld & 3) ||
+      (ld & 7) ||
       !(eps >= 0.0f) || !std::isfinite(eps))
     return INDEXER_ERR_SHAPE;
   if (tokens == 0) return INDEXER_OK;
   if (!k || !ln_w || !ln_b || !positions || (rope_dim > 0 && !cos_sin) || !token_table ||
       !block_table || !cache || !cache_scale)
     return INDEXER_ERR_NULL;
-  if (!aligned(k, 8) || !aligned(cos_sin, 4) || !aligned(ln_w, 16) || !aligned(ln_b, 16) ||
-      !aligned(cache, 4) || !aligned(cache_scale, 4) || !aligned(positions, 4) ||
+  if (!aligned(k, 16) || !aligned(cos_sin, 4) || !aligned(ln_w, 16) || !aligned(ln_b, 16) ||
+      !aligned(cache, 8) || !aligned(cache_scale, 4) || !aligned(positions, 4) ||
       !aligned(token_table, 4) || !aligned(block_table, 4) || (status && !aligned(status, 4)))
     return INDEXER_ERR_ALIGN;
-  Params p{k, ld, tokens, ln_w, ln_b, eps, positions, cos_sin, max_pos, rope_dim, token_table,
-           block_table, n_tables, table_ld, page_size, cache, cache_scale, num_slots, status};
-  const int64_t blocks = ((int64_t)tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  int shift = -1;
+  if ((page_size & (page_size - 1)) == 0)
+    for (shift = 0; (1 << shift) < page_size; ++shift) {
+    }
+  Params p{k,           ld,          tokens,   ln_w,      ln_b,  eps,         positions,
+           cos_sin,     max_pos,     rope_dim, token_table, block_table, n_tables, table_ld,
+           page_size,   shift,       cache,    cache_scale, num_slots,   status};
+  const int64_t per_block = (int64_t)kWarpsPerBlock * kTokensPerWarp;
+  const int64_t blocks = ((int64_t)tokens + per_block - 1) / per_block;
   key_prologue_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? INDEXER_OK : INDEXER_ERR_CUDA;
 }

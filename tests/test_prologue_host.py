@@ -36,13 +36,13 @@ def test_argument_errors_before_any_launch():
     assert _call(lib, table_ld=0) == shape
     assert _call(lib, num_slots=-1) == shape
     assert _call(lib, ld=100) == shape
-    assert _call(lib, ld=130) == shape          # not a multiple of 4
+    assert _call(lib, ld=132) == shape          # not a multiple of 8
     assert _call(lib, eps=-1.0) == shape
     assert _call(lib, eps=float("nan")) == shape
     assert _call(lib, tokens=0) == B.PROLOGUE_OK  # nothing to do
     assert _call(lib, k=None) == B.PROLOGUE_ERR_NULL
     assert _call(lib, cache_scale=None) == B.PROLOGUE_ERR_NULL
-    assert _call(lib, k=0x1004) == B.PROLOGUE_ERR_ALIGN      # k needs 8 bytes
+    assert _call(lib, k=0x1008) == B.PROLOGUE_ERR_ALIGN      # k needs 16 bytes
     assert _call(lib, ln_w=0x2008) == B.PROLOGUE_ERR_ALIGN   # ln_w needs 16 bytes
-    assert _call(lib, cache=0x8002) == B.PROLOGUE_ERR_ALIGN
+    assert _call(lib, cache=0x8004) == B.PROLOGUE_ERR_ALIGN
     assert _call(lib, status=0x9002) == B.PROLOGUE_ERR_ALIGN
