@@ -352,3 +352,104 @@ def key_prologue(seed: int = SEED_BASE + 6, reqs=((0, 16384), (4000, 4096), (100
                     rng.normal(0.0, 0.1, dim).astype(np.float32), 1e-6,
                     np.array(pos, np.int32), rope_table(max_pos, rope_dim), rope_dim,
                     np.array(t2t, np.int32), tab, page_size, int(sum(need)) * page_size)
+
+
+# ---------------------------------------------------------------- top-K resolver
+@dataclasses.dataclass
+class ResolverBatch:
+    """Requests with a mixed-residency block table, a hot buffer each, their history in
+    host memory, and a sequence of per-step top-K selections."""
+
+    name: str
+    block_table: np.ndarray   # int32 [R, table_ld]: block id (resident) or -1 (host only)
+    page_size: int
+    lens: np.ndarray          # int32 [R]: context length of each request
+    hot_rows: np.ndarray      # int32 [R, H]: KV rows of each request's hot slots
+    kv_rows: int              # rows of the KV tensor
+    row_bytes: int
+    host_kv: np.ndarray       # uint8 [sum(lens), row_bytes]: every position's KV row
+    host_base: np.ndarray     # int64 [R]: host row of position 0 of each request
+    kv_init: np.ndarray       # uint8 [kv_rows, row_bytes]: the KV tensor before step 0
+    steps: List[np.ndarray]   # int32 [R, k] per step: selected positions (distinct, -1 pad)
+
+    @property
+    def rows(self) -> int:
+        return int(self.block_table.shape[0])
+
+    @property
+    def hot_size(self) -> int:
+        return int(self.hot_rows.shape[1])
+
+
+def hisparse(seed: int = SEED_BASE + 7, reqs: int = 8, k: int = 2048, page_size: int = 64,
+             lens=None, tail: int = 4096, resident_frac: float = 0.1, row_bytes: int = 656,
+             n_steps: int = 4, keep: float = 0.85, tail_frac: float = 0.1) -> ResolverBatch:
+    """Decode steps of `reqs` requests under KV pressure. Each request keeps its last
+    `tail` positions resident plus a `resident_frac` share of older pages; the other
+    pages are null placeholders whose rows live in host memory. Each request leases a
+    hot buffer of 2k rows (whole blocks from the same pool). Step selections: about
+    `keep` of the previous step's positions again (decode attends to much the same
+    tokens from step to step), the rest new, `tail_frac` of them in the resident tail;
+    -1 padding when a request has fewer than k positions. Row bytes 656: one FP8
+    sparse-MLA token row (512 fp8 + 64 bf16 + 16 scale bytes)."""
+    rng = _rng(seed)
+    if lens is None:
+        lens = rng.integers(20000, 60000, size=reqs)
+    lens = np.asarray(lens, np.int64)
+    R = len(lens)
+    H = 2 * k
+    n_pages = -(-lens // page_size)
+    table_ld = int(n_pages.max())
+    tab = np.full((R, table_ld), -1, np.int32)
+    blocks = 0
+    for j in range(R):
+        npg = int(n_pages[j])
+        res = np.zeros(npg, bool)
+        res[max(0, npg - (-(-tail // page_size))):] = True
+        res |= rng.random(npg) < resident_frac
+        idx = np.nonzero(res)[0]
+        tab[j, idx] = np.arange(blocks, blocks + len(idx), dtype=np.int32)
+        blocks += len(idx)
+    hot_blocks = -(-H // page_size)  # whole blocks; the first H rows are the slots
+    hot_rows = np.zeros((R, H), np.int32)
+    for j in range(R):
+        base = blocks + j * hot_blocks
+        hot_rows[j] = (base * page_size + rng.permutation(H)).astype(np.int32)
+    kv_rows = (blocks + R * hot_blocks) * page_size
+    # shuffle the physical block ids so resident and hot rows interleave in the pool
+    perm = rng.permutation(blocks + R * hot_blocks).astype(np.int64)
+    tab = np.where(tab >= 0, perm[np.maximum(tab, 0)], -1).astype(np.int32)
+    hot_rows = (perm[hot_rows // page_size] * page_size + hot_rows % page_size).astype(np.int32)
+    host_base = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    host_kv = rng.integers(0, 256, size=(int(lens.sum()), row_bytes), dtype=np.uint8)
+    kv_init = rng.integers(0, 256, size=(kv_rows, row_bytes), dtype=np.uint8)
+    steps = []
+    prev = [None] * R
+    for s in range(n_steps):
+        sel = np.full((R, k), -1, np.int32)
+        for j in range(R):
+            L = int(lens[j])
+            m = min(k, L)
+            chosen: List[int] = []
+            seen = set()
+            if prev[j] is not None:
+                for p in prev[j]:
+                    if len(chosen) >= int(keep * m):
+                        break
+                    if rng.random() < keep and p not in seen:
+                        chosen.append(int(p))
+                        seen.add(int(p))
+            while len(chosen) < m:
+                if rng.random() < tail_frac:
+                    p = int(rng.integers(max(0, L - tail), L))
+                else:
+                    p = int(rng.integers(0, L))
+                if p not in seen:
+                    chosen.append(p)
+                    seen.add(p)
+            order = rng.permutation(m)
+            sel[j, :m] = np.asarray(chosen, np.int32)[order]
+            prev[j] = sel[j, :m].copy()
+        steps.append(sel)
+    return ResolverBatch("hisparse", tab, page_size, lens.astype(np.int32), hot_rows, kv_rows,
+                         row_bytes, host_kv, host_base, kv_init, steps)
