@@ -30,7 +30,9 @@ Readings taken here (the pages sketch the policy; each is also listed in DESIGN.
   hot_step = s, and host row host_base[j] + p is copied into KV row hot_rows[j, v].
 * A miss with no victim left (more misses than slots unused at this step) resolves to
   -1 and sets status bit 1. A position outside the table row or the position map sets
-  bit 2; a host row outside the host array bit 4; both resolve to -1.
+  bit 2; a host row outside the host array bit 4; a victim's KV row outside the KV
+  array bit 8. Each resolves to -1; a miss that fails takes its victim position in the
+  order but changes no state.
 """
 from __future__ import annotations
 
@@ -39,6 +41,7 @@ import numpy as np
 ERR_NO_VICTIM = 1
 ERR_POSITION = 2
 ERR_HOST_ROW = 4
+ERR_KV_ROW = 8
 
 MUTANTS = {
     1: "victims: most recently used first",
@@ -106,6 +109,9 @@ def resolve_step(positions, block_table, page_size, token_to_hot, hot_token, hot
                 err |= ERR_HOST_ROW
                 continue
             v = cand[mi]
+            if int(hot_rows[j, v]) < 0 or int(hot_rows[j, v]) >= kv.shape[0]:
+                err |= ERR_KV_ROW
+                continue
             old = int(hot_token[j, v])
             if old >= 0 and mutant != 7:
                 token_to_hot[j, old] = -1

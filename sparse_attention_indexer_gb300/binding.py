@@ -32,7 +32,7 @@ EXPORTS = (
     "topk_workspace_bytes", "topk_max_row_len", "topk_chunk_capacity", "topk_plan",
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
-    "topk_select_paged_noalloc", "indexer_k_prologue",
+    "topk_select_paged_noalloc", "indexer_k_prologue", "hisparse_resolve",
 )
 
 
@@ -65,7 +65,16 @@ _SIGS = {
     "indexer_k_prologue": (_c.c_int, [_VP, _c.c_int64, _c.c_int, _c.c_int, _VP, _VP, _c.c_float,
                                       _VP, _VP, _c.c_int, _c.c_int, _VP, _VP, _c.c_int,
                                       _c.c_int64, _c.c_int, _VP, _VP, _c.c_int64, _VP, _VP]),
+    "hisparse_resolve": (_c.c_int, [_VP, _c.c_int, _c.c_int, _VP, _c.c_int64, _c.c_int, _VP,
+                                    _c.c_int64, _VP, _VP, _VP, _c.c_int, _c.c_int, _VP, _VP,
+                                    _c.c_int64, _VP, _c.c_int64, _c.c_int, _VP, _VP, _VP, _VP]),
 }
+
+# include/hisparse_resolver.h
+RESOLVER_STATUS_NO_VICTIM = 1
+RESOLVER_STATUS_POSITION = 2
+RESOLVER_STATUS_HOST_ROW = 4
+RESOLVER_STATUS_KV_ROW = 8
 
 # include/indexer_prologue.h
 PROLOGUE_OK = 0
@@ -218,6 +227,34 @@ def indexer_k_prologue(k, ln_w, ln_b, eps: float, positions, cos_sin, rope_dim: 
         _ptr(cache), _ptr(cache_scale), int(cache.shape[0]), _ptr(status), _stream(stream))
     if code < 0:
         raise PrologueError(code)
+    return code
+
+
+class ResolverError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"hisparse_resolve: {code}")
+        self.code = code
+
+
+def hisparse_resolve(positions, block_table, page_size: int, token_to_hot, hot_token,
+                     hot_step, hot_rows, step: int, host_kv, host_base, kv, out_rows,
+                     counts=None, status=None, stream=None) -> int:
+    """hisparse_resolve of include/hisparse_resolver.h: positions / block_table /
+    token_to_hot / hot_token / hot_step / hot_rows / out_rows CUDA int32 tensors, host_kv
+    a pinned CPU uint8 tensor [host_rows, row_bytes], host_base CUDA int64 [rows], kv
+    CUDA uint8 [kv_rows, row_bytes]. Argument marshalling only."""
+    if host_kv.is_cuda or (host_kv.numel() and not host_kv.is_pinned()):
+        raise ValueError("host_kv must be pinned host memory")
+    rows, k = int(positions.shape[0]), int(positions.shape[1])
+    code = lib().hisparse_resolve(
+        _ptr(positions), rows, k, _ptr(block_table), int(block_table.stride(0)),
+        int(page_size), _ptr(token_to_hot), int(token_to_hot.stride(0)), _ptr(hot_token),
+        _ptr(hot_step), _ptr(hot_rows), int(hot_rows.shape[1]), int(step),
+        host_kv.data_ptr() or None, _ptr(host_base), int(host_kv.shape[0]), _ptr(kv),
+        int(kv.shape[0]), int(kv.shape[1]), _ptr(out_rows), _ptr(counts), _ptr(status),
+        _stream(stream))
+    if code < 0:
+        raise ResolverError(code)
     return code
 
 

@@ -1,8 +1,8 @@
 """Builds the CUDA library libtopk_paged.so in-tree for sm_103a with nvcc.
 
-Five translation units are compiled in parallel and linked into one shared library
-that exports the C ABI of include/topk_paged.h and include/indexer_prologue.h (no
-torch types cross it).
+Six translation units are compiled in parallel and linked into one shared library
+that exports the C ABI of include/topk_paged.h, include/indexer_prologue.h and
+include/hisparse_resolver.h (no torch types cross it).
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
-SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu"]
+SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu", "resolver.cu"]
 HEADERS = ["common.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -50,7 +50,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     defs = ["-DTOPK_TRACE"] if trace else []
     os.makedirs(bdir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", h)
-                                                        for h in ("topk_paged.h", "indexer_prologue.h")]
+                                                        for h in ("topk_paged.h", "indexer_prologue.h",
+                                                                  "hisparse_resolver.h")]
     objs = []
     jobs = []
     for src in SOURCES:

@@ -28,10 +28,10 @@ def _lib_or_skip():
 
 def header_exports():
     names = set()
-    for h in ("topk_paged.h", "indexer_prologue.h"):
+    for h in ("topk_paged.h", "indexer_prologue.h", "hisparse_resolver.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        names |= set(re.findall(r"\b((?:topk|indexer)_[a-z_]+)\s*\(", src))
+        names |= set(re.findall(r"\b((?:topk|indexer|hisparse)_[a-z_]+)\s*\(", src))
     return sorted(names)
 
 
@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported():
     lib = _lib_or_skip()
     names = header_exports()
     assert "topk_select_paged" in names and "topk_plan" in names
-    assert "indexer_k_prologue" in names
+    assert "indexer_k_prologue" in names and "hisparse_resolve" in names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
     assert set(names) <= set(B.EXPORTS), set(names) - set(B.EXPORTS)

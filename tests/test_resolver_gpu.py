@@ -1,0 +1,89 @@
+"""GPU parity of the fused top-K resolver (hisparse_resolve, through the C ABI) against
+the CPU oracle (oracle/resolver.py), bit-exact: after every step of a multi-step
+sequence, the resolved rows, the counts, the status bits, the hot state (position map,
+slot map, slot steps) and the whole KV tensor must match."""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import resolver as RV
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from sparse_attention_indexer_gb300 import binding as B  # noqa: E402
+
+
+def run_sequence(b, hot_rows=None, steps=None):
+    dev = torch.device("cuda", 0)
+    hot_rows = b.hot_rows if hot_rows is None else hot_rows
+    steps = b.steps if steps is None else steps
+    R, H = hot_rows.shape
+    map_ld = int(b.lens.max())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    g_t2h = torch.full((R, map_ld), -1, dtype=torch.int32, device=dev)
+    g_ht = torch.full((R, H), -1, dtype=torch.int32, device=dev)
+    g_hs = torch.full((R, H), -1, dtype=torch.int32, device=dev)
+    g_hot_rows, g_tab, g_base = t(hot_rows), t(b.block_table), t(b.host_base)
+    g_kv = t(b.kv_init)
+    host = torch.from_numpy(b.host_kv).pin_memory()
+    o_t2h = np.full((R, map_ld), -1, np.int32)
+    o_ht = np.full((R, H), -1, np.int32)
+    o_hs = np.full((R, H), -1, np.int32)
+    o_kv = b.kv_init.copy()
+    for s, sel in enumerate(steps):
+        k = sel.shape[1]
+        out = torch.full((R, k), -9, dtype=torch.int32, device=dev)
+        counts = torch.zeros((R, 3), dtype=torch.int32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        B.hisparse_resolve(t(sel), g_tab, b.page_size, g_t2h, g_ht, g_hs, g_hot_rows, s, host,
+                           g_base, g_kv, out, counts=counts, status=status)
+        torch.cuda.synchronize()
+        o_out, o_counts, o_err = RV.resolve_step(sel, b.block_table, b.page_size, o_t2h, o_ht,
+                                                 o_hs, hot_rows, s, b.host_kv, b.host_base, o_kv)
+        assert int(status.item()) == o_err, f"step {s}: status {int(status.item())} != {o_err}"
+        assert np.array_equal(out.cpu().numpy(), o_out), f"step {s}: resolved rows differ"
+        assert np.array_equal(counts.cpu().numpy(), o_counts), f"step {s}: counts differ"
+        assert np.array_equal(g_t2h.cpu().numpy(), o_t2h), f"step {s}: position map differs"
+        assert np.array_equal(g_ht.cpu().numpy(), o_ht), f"step {s}: slot map differs"
+        assert np.array_equal(g_hs.cpu().numpy(), o_hs), f"step {s}: slot steps differ"
+        assert np.array_equal(g_kv.cpu().numpy(), o_kv), f"step {s}: KV tensor differs"
+    return o_counts
+
+
+def test_small_sequence():
+    b = W.hisparse(seed=W.SEED_BASE + 71, reqs=4, k=512, lens=[20000, 30000, 5000, 300],
+                   row_bytes=64, n_steps=6)
+    run_sequence(b)
+
+
+def test_low_locality_and_many_steps():
+    b = W.hisparse(seed=W.SEED_BASE + 72, reqs=3, k=256, lens=[9000, 4000, 700], row_bytes=32,
+                   n_steps=12, keep=0.3)
+    run_sequence(b)
+
+
+def test_full_size_decode_batch():
+    """8 requests, k = 2048, hot buffers of 4096 rows of 656 bytes."""
+    b = W.hisparse(seed=W.SEED_BASE + 73, reqs=8, k=2048, n_steps=4)
+    counts = run_sequence(b)
+    assert counts[:, 1].sum() > 0 and counts[:, 2].sum() > 0  # hits and misses both occur
+
+
+def test_exhausted_hot_buffer():
+    """Half as many slots as selected positions: misses beyond the free slots fail."""
+    b = W.hisparse(seed=W.SEED_BASE + 74, reqs=2, k=128, lens=[6000, 3000], row_bytes=16,
+                   n_steps=3, tail=64)
+    run_sequence(b, hot_rows=b.hot_rows[:, :64].copy())
+
+
+def test_positions_outside_the_table():
+    b = W.hisparse(seed=W.SEED_BASE + 75, reqs=2, k=64, lens=[3000, 1000], row_bytes=16,
+                   n_steps=2)
+    steps = [x.copy() for x in b.steps]
+    steps[1][0, 3] = b.block_table.shape[1] * b.page_size + 5  # past the table row
+    steps[1][1, 0] = int(b.lens.max()) + 1                      # past the position map
+    run_sequence(b, steps=steps)
