@@ -5,9 +5,11 @@
 // One CTA per request. Its threads classify the selected positions (resident, hit with
 // the slot's step refreshed, miss); a block scan ranks the misses in output order;
 // when there are any, the CTA sorts the (last step, slot) keys of the slots unused at
-// this step in shared memory (bitonic sort, at most 4096 keys), hands miss r victim r,
-// updates the two maps, and copies the missed rows from pinned host memory (read
-// directly by the kernel, 16 bytes per thread per chunk) into the victims' KV rows.
+// this step in shared memory (bitonic sort by pairs, at most 4096 keys), hands miss r
+// victim r, updates the two maps, and copies the missed rows from pinned host memory
+// (read directly by the kernel, eight 16-byte chunks per thread in flight) into the
+// victims' KV rows. Every phase issues its independent loads together: one CTA per
+// request leaves little other parallelism to hide their latency.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -89,30 +91,45 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   const int32_t* hrows = p.hot_rows + (int64_t)j * p.hot;
   int err = 0, n_res = 0, n_hit = 0;
 
-  // 1. classify; hits refresh their slot (distinct positions -> distinct slots)
-  for (int i = threadIdx.x; i < p.k; i += kThreads) {
-    const int q = pos[i];
+  // 1. classify; hits refresh their slot (distinct positions -> distinct slots). Each
+  // thread takes entries t, t + 512, t + 1024, t + 1536 and issues each level of its
+  // dependent loads (position, page entry, position map, hot row) for all four before
+  // it waits on any.
+  constexpr int kE = kMaxK / kThreads;
+  int q[kE], pg[kE], b[kE], h[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kThreads;
+    q[e] = i < p.k ? pos[i] : -1;
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    pg[e] = q[e] >= 0 ? q[e] / p.page_size : 0;
+    const bool ok = q[e] >= 0 && (int64_t)pg[e] < p.table_ld && (int64_t)q[e] < p.map_ld;
+    if (q[e] >= 0 && !ok) {
+      err |= RESOLVER_STATUS_POSITION;
+      q[e] = -2;  // resolved to -1, not a miss
+    }
+    b[e] = ok ? tab[pg[e]] : -1;
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) h[e] = (q[e] >= 0 && b[e] < 0) ? t2h[q[e]] : -1;
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const int i = threadIdx.x + e * kThreads;
+    if (i >= p.k) continue;
     uint8_t miss = 0;
     int row = -1;
-    if (q >= 0) {
-      const int pg = q / p.page_size;
-      if ((int64_t)pg >= p.table_ld || (int64_t)q >= p.map_ld) {
-        err |= RESOLVER_STATUS_POSITION;
+    if (q[e] >= 0) {
+      if (b[e] >= 0) {
+        row = (int)((int64_t)b[e] * p.page_size + (q[e] - pg[e] * p.page_size));
+        ++n_res;
+      } else if (h[e] >= 0 && h[e] < p.hot) {
+        row = hrows[h[e]];
+        hstep[h[e]] = p.step;
+        ++n_hit;
       } else {
-        const int32_t b = tab[pg];
-        if (b >= 0) {
-          row = (int)((int64_t)b * p.page_size + (q - pg * p.page_size));
-          ++n_res;
-        } else {
-          const int32_t h = t2h[q];
-          if (h >= 0 && h < p.hot) {
-            row = hrows[h];
-            hstep[h] = p.step;
-            ++n_hit;
-          } else {
-            miss = 1;
-          }
-        }
+        miss = 1;
       }
     }
     out[i] = row;
@@ -132,26 +149,48 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     // 3. victim order: slots unused at this step by (last step, slot), padded to 2^n
     int n = 1;
     while (n < p.hot) n <<= 1;
-    for (int h = threadIdx.x; h < n; h += kThreads) {
-      uint64_t key = kNone;
-      if (h < p.hot) {
-        const int st = hstep[h];  // hits of this step are written above (same block)
-        if (st < p.step) key = ((uint64_t)(uint32_t)(st + 1) << 32) | (uint32_t)h;
-      }
-      s.keys[h] = key;
+    constexpr int kS = kMaxHot / kThreads;
+    int st[kS];
+#pragma unroll
+    for (int e = 0; e < kS; ++e) {  // hits of this step are written above (same block)
+      const int hh = threadIdx.x + e * kThreads;
+      st[e] = hh < p.hot ? hstep[hh] : p.step;
+    }
+#pragma unroll
+    for (int e = 0; e < kS; ++e) {
+      const int hh = threadIdx.x + e * kThreads;
+      if (hh < n)
+        s.keys[hh] = st[e] < p.step ? ((uint64_t)(uint32_t)(st[e] + 1) << 32) | (uint32_t)hh
+                                    : kNone;
     }
     __syncthreads();
+    // Bitonic sort by pairs: stage (k2, j2) compares keys i and i + j2 for every i
+    // whose bit j2 is clear, ascending where bit k2 of i is clear. Each thread takes
+    // pairs t, t + 512, ... and loads all of them before it stores any.
+    constexpr int kP = kMaxHot / 2 / kThreads;
+    const int pairs = n >> 1;
     for (int k2 = 2; k2 <= n; k2 <<= 1) {
       for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-        for (int i = threadIdx.x; i < n; i += kThreads) {
-          const int ixj = i ^ j2;
-          if (ixj > i) {
-            const uint64_t a = s.keys[i], b = s.keys[ixj];
-            const bool up = (i & k2) == 0;
-            if ((a > b) == up) {
-              s.keys[i] = b;
-              s.keys[ixj] = a;
-            }
+        uint64_t a[kP], b[kP];
+        int ia[kP];
+#pragma unroll
+        for (int e = 0; e < kP; ++e) {
+          const int pi = threadIdx.x + e * kThreads;
+          ia[e] = -1;
+          if (pi < pairs) {
+            const int i = ((pi & ~(j2 - 1)) << 1) | (pi & (j2 - 1));
+            ia[e] = i;
+            a[e] = s.keys[i];
+            b[e] = s.keys[i + j2];
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < kP; ++e) {
+          if (ia[e] < 0) continue;
+          const bool up = (ia[e] & k2) == 0;
+          if ((a[e] > b[e]) == up) {
+            s.keys[ia[e]] = b[e];
+            s.keys[ia[e] + j2] = a[e];
           }
         }
         __syncthreads();
@@ -193,14 +232,29 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     __syncthreads();
 
     // 5. copies: (miss, 16-byte chunk) pairs spread over the block
+    // eight chunks per thread in flight: loads first, then the stores
     const int chunks = p.row_bytes >> 4;
     const int64_t total = (int64_t)m * chunks;
-    for (int64_t c = threadIdx.x; c < total; c += kThreads) {
-      const int rr = (int)(c / chunks), q = (int)(c - (int64_t)rr * chunks);
-      const int64_t src = s.copy_src[rr];
-      if (src < 0) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(p.host + src * p.row_bytes + 16 * q);
-      *reinterpret_cast<uint4*>(p.kv + (int64_t)s.copy_dst[rr] * p.row_bytes + 16 * q) = v;
+    constexpr int kC = 8;
+    for (int64_t c0 = threadIdx.x; c0 < total; c0 += (int64_t)kC * kThreads) {
+      uint4 v[kC];
+      int64_t dst[kC];
+#pragma unroll
+      for (int e = 0; e < kC; ++e) {
+        const int64_t c = c0 + (int64_t)e * kThreads;
+        dst[e] = -1;
+        if (c < total) {
+          const int rr = (int)(c / chunks), cq = (int)(c - (int64_t)rr * chunks);
+          const int64_t src = s.copy_src[rr];
+          if (src >= 0) {
+            v[e] = *reinterpret_cast<const uint4*>(p.host + src * p.row_bytes + 16 * cq);
+            dst[e] = (int64_t)s.copy_dst[rr] * p.row_bytes + 16 * cq;
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kC; ++e)
+        if (dst[e] >= 0) *reinterpret_cast<uint4*>(p.kv + dst[e]) = v[e];
     }
   }
 
