@@ -49,6 +49,9 @@ struct Params {
 
 struct Smem {
   uint64_t keys[kMaxHot];     // victim order: (hot_step + 1) << 32 | slot, kNone excluded
+  uint64_t vkeys[kMaxK];      // the victims' keys, sorted (selection path)
+  uint32_t hist[256];
+  int32_t sel[8];
   int32_t miss_entry[kMaxK];  // entry index of the miss of each rank
   uint8_t is_miss[kMaxK];
   int64_t copy_src[kMaxK];    // host row of each assigned miss (by rank), -1 none
@@ -164,9 +167,124 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
                                     : kNone;
     }
     __syncthreads();
-    // Bitonic sort by pairs: stage (k2, j2) compares keys i and i + j2 for every i
-    // whose bit j2 is clear, ascending where bit k2 of i is clear. Each thread takes
-    // pairs t, t + 512, ... and loads all of them before it stores any.
+    // The misses need only the m oldest keys. When the candidates' steps span less than
+    // 2^20, each key fits 32 bits ((step - oldest step) << 12 | slot, unique): a radix
+    // select in four 8-bit passes finds the m-th smallest, the keys up to it are
+    // compacted (exactly min(m, candidates) of them) and only those are sorted. Else
+    // every key is sorted.
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    int ncand = 0;
+#pragma unroll
+    for (int e = 0; e < kS; ++e) {
+      const int hh = threadIdx.x + e * kThreads;
+      if (hh < n && s.keys[hh] != kNone) {
+        const uint32_t stp = (uint32_t)(s.keys[hh] >> 32);
+        lo = min(lo, stp);
+        hi = max(hi, stp);
+        ++ncand;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      s.red[0][threadIdx.x >> 5] = (int)lo;
+      s.red[1][threadIdx.x >> 5] = (int)hi;
+      s.red[2][threadIdx.x >> 5] = ncand;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t l = 0xFFFFFFFFu, h2 = 0u;
+      int c = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        l = min(l, (uint32_t)s.red[0][w]);
+        h2 = max(h2, (uint32_t)s.red[1][w]);
+        c += s.red[2][w];
+      }
+      s.sel[0] = (int)l;
+      s.sel[1] = (int)h2;
+      s.sel[2] = c;
+    }
+    __syncthreads();
+    const uint32_t base = (uint32_t)s.sel[0];
+    const int cand = s.sel[2];
+    const int want = min(m, cand);  // victims to hand out
+    const bool small = cand > 0 && (uint32_t)s.sel[1] - base < (1u << 20);
+    uint64_t* victims = s.keys;  // sorted victim keys, victims[0 .. want)
+    if (small && want > 0) {
+      auto key32 = [&](uint64_t k64) -> uint32_t {
+        return (((uint32_t)(k64 >> 32) - base) << 12) | ((uint32_t)k64 & 0xFFFu);
+      };
+      uint32_t prefix = 0u, mask = 0u;
+      int need = want;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += kThreads) s.hist[i] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < kS; ++e) {
+          const int hh = threadIdx.x + e * kThreads;
+          if (hh < n && s.keys[hh] != kNone) {
+            const uint32_t k = key32(s.keys[hh]);
+            if ((k & mask) == prefix) atomicAdd(&s.hist[(k >> shift) & 255u], 1u);
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {  // digit where the running count reaches `need`
+          const int lane = threadIdx.x;
+          int c[8], tot = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            c[q] = (int)s.hist[8 * lane + q];
+            tot += c[q];
+          }
+          int incl = tot;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int before = incl - tot;
+          if (before < need && need <= incl) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (before + c[q] >= need) {
+                s.sel[3] = 8 * lane + q;
+                s.sel[4] = need - before;
+                break;
+              }
+              before += c[q];
+            }
+          }
+        }
+        __syncthreads();
+        prefix |= (uint32_t)s.sel[3] << shift;
+        mask |= 255u << shift;
+        need = s.sel[4];
+        __syncthreads();
+      }
+      // compact the victims (key32 <= prefix: exactly `want` keys), then sort them
+      if (threadIdx.x == 0) s.sel[5] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < kS; ++e) {
+        const int hh = threadIdx.x + e * kThreads;
+        if (hh < n && s.keys[hh] != kNone && key32(s.keys[hh]) <= prefix)
+          s.vkeys[atomicAdd(&s.sel[5], 1)] = s.keys[hh];
+      }
+      __syncthreads();
+      int nv = 1;
+      while (nv < want) nv <<= 1;
+      for (int i = want + threadIdx.x; i < nv; i += kThreads) s.vkeys[i] = kNone;
+      __syncthreads();
+      victims = s.vkeys;
+      n = nv;
+    }
+    // Bitonic sort by pairs of victims[0 .. n): stage (k2, j2) compares keys i and
+    // i + j2 for every i whose bit j2 is clear, ascending where bit k2 of i is clear.
+    // Each thread takes pairs t, t + 512, ... and loads all of them before it stores.
     constexpr int kP = kMaxHot / 2 / kThreads;
     const int pairs = n >> 1;
     for (int k2 = 2; k2 <= n; k2 <<= 1) {
@@ -180,8 +298,8 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
           if (pi < pairs) {
             const int i = ((pi & ~(j2 - 1)) << 1) | (pi & (j2 - 1));
             ia[e] = i;
-            a[e] = s.keys[i];
-            b[e] = s.keys[i + j2];
+            a[e] = victims[i];
+            b[e] = victims[i + j2];
           }
         }
 #pragma unroll
@@ -189,8 +307,8 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
           if (ia[e] < 0) continue;
           const bool up = (ia[e] & k2) == 0;
           if ((a[e] > b[e]) == up) {
-            s.keys[ia[e]] = b[e];
-            s.keys[ia[e] + j2] = a[e];
+            victims[ia[e]] = b[e];
+            victims[ia[e] + j2] = a[e];
           }
         }
         __syncthreads();
@@ -204,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
       const int q = pos[i];
       s.copy_src[rr] = -1;
       s.copy_dst[rr] = -1;
-      const uint64_t key = rr < n ? s.keys[rr] : kNone;
+      const uint64_t key = rr < want ? victims[rr] : kNone;
       if (key == kNone) {
         err |= RESOLVER_STATUS_NO_VICTIM;
         continue;
