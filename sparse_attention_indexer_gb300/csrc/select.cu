@@ -285,17 +285,16 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 }
 
 // Row barriers among the G CTAs of a row, as an arrival and a wait (a CTA can work
-// in between). All threads call both. At arrival, a thread that wrote row state to
-// global memory (histogram reductions, candidates) passes wrote = true and fences its
-// own writes first, so that they are performed before thread 0 arrives (an arrival by
-// one thread does not order other warps' writes still in flight); thread 0 then
-// release-stores its rank's flag, (barriers passed) << 32 | payload. The wait has the
+// in between). All threads call both. At arrival the CTA barrier orders every
+// thread's earlier global writes (histogram reductions, candidates) before thread 0's
+// gpu-scope fence, which is cumulative in the PTX memory model: one fence by thread 0
+// after the barrier publishes the whole CTA's writes, and thread 0 then release-stores
+// its rank's flag, (barriers passed) << 32 | payload. The wait has the
 // lanes of warp 0 acquire every rank's flag; afterwards s.pay[j] holds rank j's
 // payload, *prefix (if non-null) the sum of the payloads of ranks below this one and
 // s.bc[18] the largest payload. group_wait returns false if a bounded wait expired
 // (status set).
-__device__ uint32_t group_arrive(Unit& u, bool wrote, uint32_t payload) {
-  if (wrote) __threadfence();
+__device__ uint32_t group_arrive(Unit& u, uint32_t payload) {
   __syncthreads();
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0 && u.bar_seq == 0) g_select_trace[blockIdx.x * 32 + 26] = global_timer_ns();
@@ -358,8 +357,8 @@ __device__ bool group_wait(Ctx& c, Unit& u, uint32_t my, int* prefix) {
   return c.s.bc[15] != 0;
 }
 
-__device__ bool group_sync(Ctx& c, Unit& u, bool wrote, uint32_t payload, int* prefix) {
-  return group_wait(c, u, group_arrive(u, wrote, payload), prefix);
+__device__ bool group_sync(Ctx& c, Unit& u, uint32_t payload, int* prefix) {
+  return group_wait(c, u, group_arrive(u, payload), prefix);
 }
 
 // Finds bin b of a 4096-bin histogram (8 bins per thread: row-wide counts g[], this
@@ -450,14 +449,10 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
       blocal = s.bc[0];
     }
     u.blocal = blocal;
-    bool wrote = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (loc[j] && b0 + j >= blocal) {
-        red_add_u32(&ghist[b0 + j], loc[j]);
-        wrote = true;
-      }
-    if (!group_sync(c, u, wrote, 0u, nullptr)) return false;
+      if (loc[j] && b0 + j >= blocal) red_add_u32(&ghist[b0 + j], loc[j]);
+    if (!group_sync(c, u, 0u, nullptr)) return false;
     if (b0 + 7 >= blocal) {
       load8_cg(&ghist[b0], glob);
     } else {
@@ -505,13 +500,9 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
     }
     u.blocal = blocal;
     TOPK_MARK(g_select_trace, 24);
-    bool wrote = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (loc[j] && t + j >= blocal) {
-        red_add_u32(&u.gs->hist0[t + j], loc[j]);
-        wrote = true;
-      }
+      if (loc[j] && t + j >= blocal) red_add_u32(&u.gs->hist0[t + j], loc[j]);
 #ifdef TOPK_TRACE
     {
       int nw = 0;
@@ -520,7 +511,7 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
       if ((threadIdx.x & 31) == 0) atomicAdd(&s.bc[30], nw);
     }
 #endif
-    if (!group_sync(c, u, wrote, (uint32_t)blocal, nullptr)) return false;
+    if (!group_sync(c, u, (uint32_t)blocal, nullptr)) return false;
     TOPK_MARK(g_select_trace, 25);
     const int top = s.bc[18];
     if (t + 7 >= blocal) {
@@ -534,15 +525,11 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
     const bool complete = s.bc[0] >= top;
     __syncthreads();
     if (!complete) {
-      wrote = false;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (loc[j] && t + j < blocal) {
-          red_add_u32(&u.gs->hist0[t + j], loc[j]);
-          wrote = true;
-        }
+        if (loc[j] && t + j < blocal) red_add_u32(&u.gs->hist0[t + j], loc[j]);
       u.blocal = 0;
-      if (!group_sync(c, u, wrote, 0u, nullptr)) return false;
+      if (!group_sync(c, u, 0u, nullptr)) return false;
       load8_cg(&u.gs->hist0[t], glob);
       find_threshold(glob, loc, need, s);
     }
@@ -893,7 +880,7 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, 
       int ob = emitted;
       if (u.G > 1) {
         int pre;
-        if (!group_sync(c, u, false, (uint32_t)(lal + (take ? lel : 0)), &pre)) return false;
+        if (!group_sync(c, u, (uint32_t)(lal + (take ? lel : 0)), &pre)) return false;
         for (int i = threadIdx.x; i < kBins0; i += kThreads) u.gs->hlev[lev][i] = 0u;
         ob += pre;
       }
@@ -924,7 +911,7 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, 
   const uint32_t T = pval;
   int prefix = 0;
   if (u.G > 1) {
-    if (!group_sync(c, u, false, (uint32_t)local_tie, &prefix)) return false;
+    if (!group_sync(c, u, (uint32_t)local_tie, &prefix)) return false;
     passed_barrier();
   }
   const int tie_base = emitted;  // every other entry fills [0, emitted)
@@ -1241,7 +1228,6 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   // for every rank to fit its slot; otherwise candidates wait for the offsets.
   const int slot_cap = u.G > 1 ? kGroupCap / u.G : 0;
   const bool slots = compact && u.G > 1 && eq0 <= slot_cap;
-  bool wrote_cand = false;
   auto write_candidates = [&](int base) {
     // staged list, or an ordered second pass straight to global
     if (stage_cand) {
@@ -1250,7 +1236,6 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         if (base + i < kGroupCap) {
           u.gs->cand_key[base + i] = s.u.l.ckey[i];
           u.gs->cand_pos[base + i] = s.u.l.cpos[i];
-          wrote_cand = true;
         }
     } else {
       int cnt = 0;
@@ -1275,7 +1260,6 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
             if (gi < kGroupCap) {
               u.gs->cand_key[gi] = f2key(xs[j]);
               u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
-              wrote_cand = true;
             }
             ++gi;
           }
@@ -1300,7 +1284,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const bool overlap = u.G > 1 && !fallback && !(compact && !slots && !stage_cand);
   int out_base = 0, cand_base = 0;
   if (overlap) {
-    const uint32_t seq = group_arrive(u, wrote_cand, counts);
+    const uint32_t seq = group_arrive(u, counts);
     for (int i = threadIdx.x; i < n_emit; i += kThreads)
       slot_e[i] = lookup_slot(c, u, s.u.l.elist[i]);
     for (int i = threadIdx.x; i < n_own; i += kThreads)
@@ -1332,7 +1316,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
         atomicOr(&u.gs->or_key, fo);
       }
       int pre;
-      if (!group_sync(c, u, wrote_cand || (fallback && threadIdx.x == 0), counts, &pre)) return;
+      if (!group_sync(c, u, counts, &pre)) return;
       for (int i = u.blocal + threadIdx.x; i < kBins0; i += kThreads) u.gs->hist0[i] = 0u;
       out_base = pre & 0xFFFF;
       cand_base = pre >> 16;
@@ -1391,7 +1375,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       }
     } else {
       write_candidates(cand_base);
-      if (!group_sync(c, u, wrote_cand, 0u, nullptr)) return;
+      if (!group_sync(c, u, 0u, nullptr)) return;
       for (int i = threadIdx.x; i < n; i += kThreads) {
         lkey[i] = __ldcg(&u.gs->cand_key[i]);
         lpos[i] = __ldcg(&u.gs->cand_pos[i]);
