@@ -287,13 +287,13 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 // Row barriers among the G CTAs of a row, as an arrival and a wait (a CTA can work
 // in between). All threads call both. At arrival the CTA barrier orders every
 // thread's earlier global writes (histogram reductions, candidates) before thread 0's
-// gpu-scope fence, which is cumulative in the PTX memory model: one fence by thread 0
-// after the barrier publishes the whole CTA's writes, and thread 0 then release-stores
-// its rank's flag, (barriers passed) << 32 | payload. The wait has the
-// lanes of warp 0 acquire every rank's flag; afterwards s.pay[j] holds rank j's
-// payload, *prefix (if non-null) the sum of the payloads of ranks below this one and
-// s.bc[18] the largest payload. group_wait returns false if a bounded wait expired
-// (status set).
+// gpu-scope release store of its rank's flag, (barriers passed) << 32 | payload. A
+// release is cumulative in the PTX memory model, so that one store publishes the
+// whole CTA's writes to a rank that acquires the flag; no thread needs its own fence.
+// The wait has the lanes of warp 0 acquire every rank's flag, then a CTA barrier
+// passes the ordering on; afterwards s.pay[j] holds rank j's payload, *prefix (if
+// non-null) the sum of the payloads of ranks below this one and s.bc[18] the largest
+// payload. group_wait returns false if a bounded wait expired (status set).
 __device__ uint32_t group_arrive(Unit& u, uint32_t payload) {
   __syncthreads();
 #ifdef TOPK_TRACE
@@ -302,7 +302,6 @@ __device__ uint32_t group_arrive(Unit& u, uint32_t payload) {
   u.bar_seq += 1;
   const uint32_t my = u.flag_base + u.bar_seq;
   if (threadIdx.x == 0) {
-    __threadfence();
     st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
   }
   return my;
