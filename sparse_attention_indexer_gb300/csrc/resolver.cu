@@ -4,9 +4,10 @@
 //
 // One CTA per request. Its threads classify the selected positions (resident, hit with
 // the slot's step refreshed, miss); a block scan ranks the misses in output order;
-// when there are any, the CTA sorts the (last step, slot) keys of the slots unused at
-// this step in shared memory (bitonic sort by pairs, at most 4096 keys), hands miss r
-// victim r, updates the two maps, and copies the missed rows from pinned host memory
+// when there are any, the CTA orders the slots unused at this step by (last step, slot)
+// (a counting order over the eight oldest step values when the victims lie there, else
+// a radix select of the victims and a bitonic sort of those), hands miss r victim r,
+// updates the two maps, and copies the missed rows from pinned host memory
 // (read directly by the kernel, eight 16-byte chunks per thread in flight) into the
 // victims' KV rows. Every phase issues its independent loads together: one CTA per
 // request leaves little other parallelism to hide their latency.
@@ -57,6 +58,7 @@ struct Smem {
   int64_t copy_src[kMaxK];    // host row of each assigned miss (by rank), -1 none
   int32_t copy_dst[kMaxK];    // KV row
   int32_t wsum[kThreads / 32];
+  uint64_t wsum2[2][kThreads / 32];
   int32_t red[4][kThreads / 32];
 };
 
@@ -149,172 +151,279 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     if (s.is_miss[i]) s.miss_entry[r++] = i;
 
   if (m > 0) {
-    // 3. victim order: slots unused at this step by (last step, slot), padded to 2^n
-    int n = 1;
-    while (n < p.hot) n <<= 1;
-    constexpr int kS = kMaxHot / kThreads;
-    int st[kS];
+    int want = 0;
+    uint64_t* victims = s.vkeys;
+    // 3. victim order: the slots unused at this step, by (last step, slot). Thread t
+    // holds slots 8t .. 8t + 7. Keyed by d = last step + 1 - (oldest such value), the
+    // order is a stable counting sort on d in slot order: a slot's rank is the number
+    // of candidates with a smaller d, plus those with its d in lower slots. One block
+    // scan of per-thread counts for d < 8 gives every rank when the victims all lie
+    // there (the usual LRU case: they come from the oldest few steps); otherwise the
+    // general order below runs.
+    constexpr int kV = kMaxHot / kThreads;
+    static_assert(kV == 8, "8 slots per thread: 4-bit counters, 8 counted offsets");
+    const int h0 = threadIdx.x * kV;
+    int sv[kV];
 #pragma unroll
-    for (int e = 0; e < kS; ++e) {  // hits of this step are written above (same block)
-      const int hh = threadIdx.x + e * kThreads;
-      st[e] = hh < p.hot ? hstep[hh] : p.step;
-    }
-#pragma unroll
-    for (int e = 0; e < kS; ++e) {
-      const int hh = threadIdx.x + e * kThreads;
-      if (hh < n)
-        s.keys[hh] = st[e] < p.step ? ((uint64_t)(uint32_t)(st[e] + 1) << 32) | (uint32_t)hh
-                                    : kNone;
-    }
-    __syncthreads();
-    // The misses need only the m oldest keys. When the candidates' steps span less than
-    // 2^20, each key fits 32 bits ((step - oldest step) << 12 | slot, unique): a radix
-    // select in four 8-bit passes finds the m-th smallest, the keys up to it are
-    // compacted (exactly min(m, candidates) of them) and only those are sorted. Else
-    // every key is sorted.
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int e = 0; e < kV; ++e) sv[e] = h0 + e < p.hot ? hstep[h0 + e] : p.step;
+    uint32_t lo = 0xFFFFFFFFu;
     int ncand = 0;
 #pragma unroll
-    for (int e = 0; e < kS; ++e) {
-      const int hh = threadIdx.x + e * kThreads;
-      if (hh < n && s.keys[hh] != kNone) {
-        const uint32_t stp = (uint32_t)(s.keys[hh] >> 32);
-        lo = min(lo, stp);
-        hi = max(hi, stp);
+    for (int e = 0; e < kV; ++e)
+      if (sv[e] < p.step) {
+        lo = min(lo, (uint32_t)(sv[e] + 1));
         ++ncand;
       }
-    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
       ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
     }
     if ((threadIdx.x & 31) == 0) {
       s.red[0][threadIdx.x >> 5] = (int)lo;
-      s.red[1][threadIdx.x >> 5] = (int)hi;
       s.red[2][threadIdx.x >> 5] = ncand;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t l = 0xFFFFFFFFu, h2 = 0u;
-      int c = 0;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        l = min(l, (uint32_t)s.red[0][w]);
-        h2 = max(h2, (uint32_t)s.red[1][w]);
-        c += s.red[2][w];
+    lo = 0xFFFFFFFFu;
+    int cand = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      lo = min(lo, (uint32_t)s.red[0][w]);
+      cand += s.red[2][w];
+    }
+    want = min(m, cand);
+    // per-thread counts of d = 0 .. 7 (4 bits each), widened to 16-bit fields of two
+    // words for the block scan (totals <= 4096)
+    uint32_t c4 = 0u;
+#pragma unroll
+    for (int e = 0; e < kV; ++e) {
+      const uint32_t d = (uint32_t)(sv[e] + 1) - lo;
+      if (sv[e] < p.step && d < 8u) c4 += 1u << (4u * d);
+    }
+    uint64_t wa = 0ull, wb = 0ull;
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+      wa |= (uint64_t)((c4 >> (4 * d)) & 15u) << (16 * d);
+      wb |= (uint64_t)((c4 >> (4 * d + 16)) & 15u) << (16 * d);
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint64_t xa = wa, xb = wb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t ya = __shfl_up_sync(0xffffffffu, xa, o);
+      const uint64_t yb = __shfl_up_sync(0xffffffffu, xb, o);
+      if (lane >= o) {
+        xa += ya;
+        xb += yb;
       }
-      s.sel[0] = (int)l;
-      s.sel[1] = (int)h2;
-      s.sel[2] = c;
+    }
+    if (lane == 31) {
+      s.wsum2[0][w] = xa;
+      s.wsum2[1][w] = xb;
     }
     __syncthreads();
-    const uint32_t base = (uint32_t)s.sel[0];
-    const int cand = s.sel[2];
-    const int want = min(m, cand);  // victims to hand out
-    const bool small = cand > 0 && (uint32_t)s.sel[1] - base < (1u << 20);
-    uint64_t* victims = s.keys;  // sorted victim keys, victims[0 .. want)
-    if (small && want > 0) {
-      auto key32 = [&](uint64_t k64) -> uint32_t {
-        return (((uint32_t)(k64 >> 32) - base) << 12) | ((uint32_t)k64 & 0xFFFu);
-      };
-      uint32_t prefix = 0u, mask = 0u;
-      int need = want;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kThreads) s.hist[i] = 0u;
-        __syncthreads();
+    uint64_t ba = xa - wa, bb = xb - wb, ta = 0ull, tb = 0ull;
 #pragma unroll
-        for (int e = 0; e < kS; ++e) {
-          const int hh = threadIdx.x + e * kThreads;
-          if (hh < n && s.keys[hh] != kNone) {
-            const uint32_t k = key32(s.keys[hh]);
-            if ((k & mask) == prefix) atomicAdd(&s.hist[(k >> shift) & 255u], 1u);
-          }
-        }
-        __syncthreads();
-        if (threadIdx.x < 32) {  // digit where the running count reaches `need`
-          const int lane = threadIdx.x;
-          int c[8], tot = 0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            c[q] = (int)s.hist[8 * lane + q];
-            tot += c[q];
-          }
-          int incl = tot;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          int before = incl - tot;
-          if (before < need && need <= incl) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (before + c[q] >= need) {
-                s.sel[3] = 8 * lane + q;
-                s.sel[4] = need - before;
-                break;
-              }
-              before += c[q];
-            }
-          }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)s.sel[3] << shift;
-        mask |= 255u << shift;
-        need = s.sel[4];
-        __syncthreads();
+    for (int i = 0; i < kThreads / 32; ++i) {
+      if (i < w) {
+        ba += s.wsum2[0][i];
+        bb += s.wsum2[1][i];
       }
-      // compact the victims (key32 <= prefix: exactly `want` keys), then sort them
-      if (threadIdx.x == 0) s.sel[5] = 0;
-      __syncthreads();
+      ta += s.wsum2[0][i];
+      tb += s.wsum2[1][i];
+    }
+    // first rank of offset d (the totals of the offsets below it) plus this thread's
+    // exclusive prefix, per 16-bit field: exclusive prefix sums inside a word by
+    // shifted adds (no field exceeds 2 * 4096)
+    constexpr uint64_t kOnes = 0x0001000100010001ull;
+    const uint64_t total_a = ((ta * kOnes) >> 48) & 0xFFFFull;
+    const int run = (int)(total_a + (((tb * kOnes) >> 48) & 0xFFFFull));
+    const uint64_t fa = (ta << 16) + (ta << 32) + (ta << 48) + ba;
+    const uint64_t fb = total_a * kOnes + (tb << 16) + (tb << 32) + (tb << 48) + bb;
+    const bool fast = run >= want;  // the same in every thread
+    if (fast) {
+      uint32_t seen = 0u;  // this thread's earlier candidates per offset (4 bits each)
 #pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        const uint32_t d = (uint32_t)(sv[e] + 1) - lo;
+        if (sv[e] < p.step && d < 8u) {
+          const int rank = (int)(((d < 4u ? fa : fb) >> (16u * (d & 3u))) & 0xFFFFull) +
+                           (int)((seen >> (4u * d)) & 15u);
+          seen += 1u << (4u * d);
+          if (rank < want)
+            s.vkeys[rank] = ((uint64_t)(uint32_t)(sv[e] + 1) << 32) | (uint32_t)(h0 + e);
+        }
+      }
+      victims = s.vkeys;
+      __syncthreads();
+    } else {
+      // General order: slots unused at this step by (last step, slot), padded to 2^n
+      int n = 1;
+      while (n < p.hot) n <<= 1;
+      constexpr int kS = kMaxHot / kThreads;
+      int st[kS];
+  #pragma unroll
+      for (int e = 0; e < kS; ++e) {  // hits of this step are written above (same block)
+        const int hh = threadIdx.x + e * kThreads;
+        st[e] = hh < p.hot ? hstep[hh] : p.step;
+      }
+  #pragma unroll
       for (int e = 0; e < kS; ++e) {
         const int hh = threadIdx.x + e * kThreads;
-        if (hh < n && s.keys[hh] != kNone && key32(s.keys[hh]) <= prefix)
-          s.vkeys[atomicAdd(&s.sel[5], 1)] = s.keys[hh];
+        if (hh < n)
+          s.keys[hh] = st[e] < p.step ? ((uint64_t)(uint32_t)(st[e] + 1) << 32) | (uint32_t)hh
+                                      : kNone;
       }
       __syncthreads();
-      int nv = 1;
-      while (nv < want) nv <<= 1;
-      for (int i = want + threadIdx.x; i < nv; i += kThreads) s.vkeys[i] = kNone;
-      __syncthreads();
-      victims = s.vkeys;
-      n = nv;
-    }
-    // Bitonic sort by pairs of victims[0 .. n): stage (k2, j2) compares keys i and
-    // i + j2 for every i whose bit j2 is clear, ascending where bit k2 of i is clear.
-    // Each thread takes pairs t, t + 512, ... and loads all of them before it stores.
-    constexpr int kP = kMaxHot / 2 / kThreads;
-    const int pairs = n >> 1;
-    for (int k2 = 2; k2 <= n; k2 <<= 1) {
-      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
-        uint64_t a[kP], b[kP];
-        int ia[kP];
-#pragma unroll
-        for (int e = 0; e < kP; ++e) {
-          const int pi = threadIdx.x + e * kThreads;
-          ia[e] = -1;
-          if (pi < pairs) {
-            const int i = ((pi & ~(j2 - 1)) << 1) | (pi & (j2 - 1));
-            ia[e] = i;
-            a[e] = victims[i];
-            b[e] = victims[i + j2];
-          }
+      // The misses need only the m oldest keys. When the candidates' steps span less than
+      // 2^20, each key fits 32 bits ((step - oldest step) << 12 | slot, unique): a radix
+      // select in four 8-bit passes finds the m-th smallest, the keys up to it are
+      // compacted (exactly min(m, candidates) of them) and only those are sorted. Else
+      // every key is sorted.
+      uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+      int ncand = 0;
+  #pragma unroll
+      for (int e = 0; e < kS; ++e) {
+        const int hh = threadIdx.x + e * kThreads;
+        if (hh < n && s.keys[hh] != kNone) {
+          const uint32_t stp = (uint32_t)(s.keys[hh] >> 32);
+          lo = min(lo, stp);
+          hi = max(hi, stp);
+          ++ncand;
         }
-#pragma unroll
-        for (int e = 0; e < kP; ++e) {
-          if (ia[e] < 0) continue;
-          const bool up = (ia[e] & k2) == 0;
-          if ((a[e] > b[e]) == up) {
-            victims[ia[e]] = b[e];
-            victims[ia[e] + j2] = a[e];
+      }
+  #pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
+      }
+      if ((threadIdx.x & 31) == 0) {
+        s.red[0][threadIdx.x >> 5] = (int)lo;
+        s.red[1][threadIdx.x >> 5] = (int)hi;
+        s.red[2][threadIdx.x >> 5] = ncand;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint32_t l = 0xFFFFFFFFu, h2 = 0u;
+        int c = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+          l = min(l, (uint32_t)s.red[0][w]);
+          h2 = max(h2, (uint32_t)s.red[1][w]);
+          c += s.red[2][w];
+        }
+        s.sel[0] = (int)l;
+        s.sel[1] = (int)h2;
+        s.sel[2] = c;
+      }
+      __syncthreads();
+      const uint32_t base = (uint32_t)s.sel[0];
+      const int cand = s.sel[2];
+      want = min(m, cand);  // victims to hand out
+      const bool small = cand > 0 && (uint32_t)s.sel[1] - base < (1u << 20);
+      victims = s.keys;  // sorted victim keys, victims[0 .. want)
+      if (small && want > 0) {
+        auto key32 = [&](uint64_t k64) -> uint32_t {
+          return (((uint32_t)(k64 >> 32) - base) << 12) | ((uint32_t)k64 & 0xFFFu);
+        };
+        uint32_t prefix = 0u, mask = 0u;
+        int need = want;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = threadIdx.x; i < 256; i += kThreads) s.hist[i] = 0u;
+          __syncthreads();
+  #pragma unroll
+          for (int e = 0; e < kS; ++e) {
+            const int hh = threadIdx.x + e * kThreads;
+            if (hh < n && s.keys[hh] != kNone) {
+              const uint32_t k = key32(s.keys[hh]);
+              if ((k & mask) == prefix) atomicAdd(&s.hist[(k >> shift) & 255u], 1u);
+            }
           }
+          __syncthreads();
+          if (threadIdx.x < 32) {  // digit where the running count reaches `need`
+            const int lane = threadIdx.x;
+            int c[8], tot = 0;
+  #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              c[q] = (int)s.hist[8 * lane + q];
+              tot += c[q];
+            }
+            int incl = tot;
+  #pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            int before = incl - tot;
+            if (before < need && need <= incl) {
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                if (before + c[q] >= need) {
+                  s.sel[3] = 8 * lane + q;
+                  s.sel[4] = need - before;
+                  break;
+                }
+                before += c[q];
+              }
+            }
+          }
+          __syncthreads();
+          prefix |= (uint32_t)s.sel[3] << shift;
+          mask |= 255u << shift;
+          need = s.sel[4];
+          __syncthreads();
+        }
+        // compact the victims (key32 <= prefix: exactly `want` keys), then sort them
+        if (threadIdx.x == 0) s.sel[5] = 0;
+        __syncthreads();
+  #pragma unroll
+        for (int e = 0; e < kS; ++e) {
+          const int hh = threadIdx.x + e * kThreads;
+          if (hh < n && s.keys[hh] != kNone && key32(s.keys[hh]) <= prefix)
+            s.vkeys[atomicAdd(&s.sel[5], 1)] = s.keys[hh];
         }
         __syncthreads();
+        int nv = 1;
+        while (nv < want) nv <<= 1;
+        for (int i = want + threadIdx.x; i < nv; i += kThreads) s.vkeys[i] = kNone;
+        __syncthreads();
+        victims = s.vkeys;
+        n = nv;
       }
-    }
+      // Bitonic sort by pairs of victims[0 .. n): stage (k2, j2) compares keys i and
+      // i + j2 for every i whose bit j2 is clear, ascending where bit k2 of i is clear.
+      // Each thread takes pairs t, t + 512, ... and loads all of them before it stores.
+      constexpr int kP = kMaxHot / 2 / kThreads;
+      const int pairs = n >> 1;
+      for (int k2 = 2; k2 <= n; k2 <<= 1) {
+        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+          uint64_t a[kP], b[kP];
+          int ia[kP];
+  #pragma unroll
+          for (int e = 0; e < kP; ++e) {
+            const int pi = threadIdx.x + e * kThreads;
+            ia[e] = -1;
+            if (pi < pairs) {
+              const int i = ((pi & ~(j2 - 1)) << 1) | (pi & (j2 - 1));
+              ia[e] = i;
+              a[e] = victims[i];
+              b[e] = victims[i + j2];
+            }
+          }
+  #pragma unroll
+          for (int e = 0; e < kP; ++e) {
+            if (ia[e] < 0) continue;
+            const bool up = (ia[e] & k2) == 0;
+            if ((a[e] > b[e]) == up) {
+              victims[ia[e]] = b[e];
+              victims[ia[e] + j2] = a[e];
+            }
+          }
+          __syncthreads();
+        }
+      }
 
+    }
     // 4. miss rank r takes victim r: maps, step, output row, the copy to make
     const int64_t hb = p.host_base[j];
     for (int rr = threadIdx.x; rr < m; rr += kThreads) {
@@ -350,7 +459,8 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     __syncthreads();
 
     // 5. copies: (miss, 16-byte chunk) pairs spread over the block
-    // eight chunks per thread in flight: loads first, then the stores
+    // eight chunks per thread in flight: loads first, then the stores (more in flight per
+    // thread measured slower: the host reads of one SM do not go faster)
     const int chunks = p.row_bytes >> 4;
     const int64_t total = (int64_t)m * chunks;
     constexpr int kC = 8;

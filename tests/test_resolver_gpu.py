@@ -87,3 +87,71 @@ def test_positions_outside_the_table():
     steps[1][0, 3] = b.block_table.shape[1] * b.page_size + 5  # past the table row
     steps[1][1, 0] = int(b.lens.max()) + 1                      # past the position map
     run_sequence(b, steps=steps)
+
+
+def _crafted_state(b, step, spread, n_miss, n_hit, seed, never_used=0.1):
+    """A hot state whose slots were last used at steps spread over [0, spread) (a
+    `never_used` share never used), each used slot holding a distinct host-only position, and one
+    step's selection: n_hit of the held positions and n_miss host-only positions that no
+    slot holds (both in random order, -1 padded to k = n_hit + n_miss)."""
+    rng = np.random.default_rng(seed)
+    R, H = b.hot_rows.shape
+    map_ld = int(b.lens.max())
+    t2h = np.full((R, map_ld), -1, np.int32)
+    ht = np.full((R, H), -1, np.int32)
+    hs = np.full((R, H), -1, np.int32)
+    k = n_hit + n_miss
+    sel = np.full((R, k), -1, np.int32)
+    for j in range(R):
+        pages = np.nonzero(b.block_table[j] < 0)[0]
+        host_only = (pages[:, None] * b.page_size + np.arange(b.page_size)).ravel()
+        host_only = host_only[host_only < b.lens[j]]
+        pick = rng.permutation(host_only)
+        used = rng.random(H) >= never_used
+        held = pick[:int(used.sum())]
+        hs[j, used] = rng.integers(0, spread, int(used.sum()))
+        ht[j, used] = held
+        t2h[j, held] = np.nonzero(used)[0]
+        free = pick[int(used.sum()):]
+        chosen = np.concatenate([rng.choice(held, n_hit, replace=False), free[:n_miss]])
+        sel[j, :chosen.size] = rng.permutation(chosen)
+    return t2h, ht, hs, sel
+
+
+def _one_step_from(b, state, step):
+    dev = torch.device("cuda", 0)
+    t2h, ht, hs, sel = state
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    g_t2h, g_ht, g_hs, g_kv = t(t2h), t(ht), t(hs), t(b.kv_init)
+    host = torch.from_numpy(b.host_kv).pin_memory()
+    R, k = sel.shape
+    out = torch.full((R, k), -9, dtype=torch.int32, device=dev)
+    counts = torch.zeros((R, 3), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.hisparse_resolve(t(sel), t(b.block_table), b.page_size, g_t2h, g_ht, g_hs, t(b.hot_rows),
+                       step, host, t(b.host_base), g_kv, out, counts=counts, status=status)
+    torch.cuda.synchronize()
+    o_t2h, o_ht, o_hs, o_kv = t2h.copy(), ht.copy(), hs.copy(), b.kv_init.copy()
+    o_out, o_counts, o_err = RV.resolve_step(sel, b.block_table, b.page_size, o_t2h, o_ht, o_hs,
+                                             b.hot_rows, step, b.host_kv, b.host_base, o_kv)
+    assert int(status.item()) == o_err
+    assert np.array_equal(out.cpu().numpy(), o_out), "resolved rows differ"
+    assert np.array_equal(counts.cpu().numpy(), o_counts), "counts differ"
+    assert np.array_equal(g_t2h.cpu().numpy(), o_t2h), "position map differs"
+    assert np.array_equal(g_ht.cpu().numpy(), o_ht), "slot map differs"
+    assert np.array_equal(g_hs.cpu().numpy(), o_hs), "slot steps differ"
+    assert np.array_equal(g_kv.cpu().numpy(), o_kv), "KV tensor differs"
+    return o_counts
+
+
+@pytest.mark.parametrize("n_miss,never_used", [(40, 0.1), (500, 0.0), (1500, 0.1)])
+def test_victims_from_slots_last_used_over_many_steps(n_miss, never_used):
+    """Slot steps spread over 40 earlier steps. 40 misses take never-used slots; 500
+    misses (every slot used) take slots from the five or so oldest steps, by step and
+    then slot; 1500 misses reach slots 13 steps younger than the oldest (past the
+    counting order for the eight oldest step values: the general victim order)."""
+    b = W.hisparse(seed=W.SEED_BASE + 76, reqs=3, k=2048, lens=[60000, 40000, 30000],
+                   row_bytes=32, n_steps=1)
+    state = _crafted_state(b, 40, 40, n_miss, 200, W.SEED_BASE + 77 + n_miss, never_used)
+    counts = _one_step_from(b, state, 40)
+    assert np.all(counts[:, 2] == n_miss) and np.all(counts[:, 1] == 200)
