@@ -13,6 +13,7 @@
 // request leaves little other parallelism to hide their latency.
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "hisparse_resolver.h"
@@ -55,12 +56,15 @@ struct Smem {
   int32_t sel[8];
   int32_t miss_entry[kMaxK];  // entry index of the miss of each rank
   uint8_t is_miss[kMaxK];
+  uint8_t hit_slot[kMaxHot];  // slots refreshed by a hit of this step
   int64_t copy_src[kMaxK];    // host row of each assigned miss (by rank), -1 none
   int32_t copy_dst[kMaxK];    // KV row
   int32_t wsum[kThreads / 32];
   uint64_t wsum2[2][kThreads / 32];
   int32_t red[4][kThreads / 32];
 };
+
+static_assert(offsetof(Smem, hit_slot) % 8 == 0, "hit bitmap zeroed with 8-byte stores");
 
 __device__ int block_excl_scan(int v, int* total, Smem& s) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -96,12 +100,25 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   const int32_t* hrows = p.hot_rows + (int64_t)j * p.hot;
   int err = 0, n_res = 0, n_hit = 0;
 
+  // The slots' last steps (for the victim order) do not depend on the classification:
+  // thread t reads those of slots 8t .. 8t + 7 now, and the hits found below are
+  // marked in a shared bitmap instead of being read back.
+  constexpr int kV = kMaxHot / kThreads;
+  static_assert(kV == 8, "8 slots per thread: 4-bit counters, 8 counted offsets");
+  const int h0 = threadIdx.x * kV;
+  reinterpret_cast<uint2*>(s.hit_slot)[threadIdx.x] = make_uint2(0u, 0u);
+  __syncthreads();
+  int sv[kV];
+#pragma unroll
+  for (int e = 0; e < kV; ++e) sv[e] = h0 + e < p.hot ? hstep[h0 + e] : p.step;
+
   // 1. classify; hits refresh their slot (distinct positions -> distinct slots). Each
   // thread takes entries t, t + 512, t + 1024, t + 1536 and issues each level of its
-  // dependent loads (position, page entry, position map, hot row) for all four before
-  // it waits on any.
+  // dependent loads for all four before it waits on any: the position; its page entry
+  // and its position-map entry together (the map is read for resident positions too,
+  // so that it does not wait on the page entry); the hot row of a hit.
   constexpr int kE = kMaxK / kThreads;
-  int q[kE], pg[kE], b[kE], h[kE];
+  int q[kE], pg[kE], b[kE], h[kE], hr[kE];
 #pragma unroll
   for (int e = 0; e < kE; ++e) {
     const int i = threadIdx.x + e * kThreads;
@@ -116,9 +133,14 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
       q[e] = -2;  // resolved to -1, not a miss
     }
     b[e] = ok ? tab[pg[e]] : -1;
+    h[e] = ok ? t2h[q[e]] : -1;
   }
 #pragma unroll
-  for (int e = 0; e < kE; ++e) h[e] = (q[e] >= 0 && b[e] < 0) ? t2h[q[e]] : -1;
+  for (int e = 0; e < kE; ++e) {
+    const bool hit = q[e] >= 0 && b[e] < 0 && h[e] >= 0 && h[e] < p.hot;
+    if (!hit) h[e] = -1;
+    hr[e] = hit ? hrows[h[e]] : -1;
+  }
 #pragma unroll
   for (int e = 0; e < kE; ++e) {
     const int i = threadIdx.x + e * kThreads;
@@ -129,9 +151,10 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
       if (b[e] >= 0) {
         row = (int)((int64_t)b[e] * p.page_size + (q[e] - pg[e] * p.page_size));
         ++n_res;
-      } else if (h[e] >= 0 && h[e] < p.hot) {
-        row = hrows[h[e]];
+      } else if (h[e] >= 0) {
+        row = hr[e];
         hstep[h[e]] = p.step;
+        s.hit_slot[h[e]] = 1;
         ++n_hit;
       } else {
         miss = 1;
@@ -160,12 +183,9 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     // scan of per-thread counts for d < 8 gives every rank when the victims all lie
     // there (the usual LRU case: they come from the oldest few steps); otherwise the
     // general order below runs.
-    constexpr int kV = kMaxHot / kThreads;
-    static_assert(kV == 8, "8 slots per thread: 4-bit counters, 8 counted offsets");
-    const int h0 = threadIdx.x * kV;
-    int sv[kV];
 #pragma unroll
-    for (int e = 0; e < kV; ++e) sv[e] = h0 + e < p.hot ? hstep[h0 + e] : p.step;
+    for (int e = 0; e < kV; ++e)
+      if (s.hit_slot[h0 + e]) sv[e] = p.step;  // used at this step: not a candidate
     uint32_t lo = 0xFFFFFFFFu;
     int ncand = 0;
 #pragma unroll
