@@ -17,6 +17,7 @@ host cores on the same workload, metric and unit.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -141,10 +142,11 @@ class _Batch:
     """Device copies of one workload batch, its plan object and two CUDA graphs: the
     whole step (plan + select) and select alone."""
 
-    def __init__(self, b, dev):
+    def __init__(self, b, dev, k=None):
         import torch
         from sparse_attention_indexer_gb300 import PagedTopK
-        self.b = b
+        self.b = b if k is None else dataclasses.replace(b, k=int(k))
+        b = self.b
         self.scores = torch.from_numpy(b.scores).to(dev)
         self.lens = torch.from_numpy(b.lens).to(dev)
         self.table = torch.from_numpy(b.block_table).to(dev)
@@ -312,6 +314,54 @@ def _time(fn, steps, flush):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def _stats_us(ms):
+    """Median and [p10, p90] of per-call times given in ms, in us."""
+    a = np.asarray(ms, np.float64) * 1e3
+    return (round(float(np.median(a)), 2),
+            [round(float(np.percentile(a, 10)), 2), round(float(np.percentile(a, 90)), 2)])
+
+
+def _time_configs(dev, flush, n_calls):
+    """plan + select of every other workload config as one CUDA graph per call, L2
+    flushed before each call: median [p10, p90] us per call and rows/s. Each call's
+    status is checked first."""
+    from sparse_attention_indexer_gb300 import binding as Bd
+    import torch
+
+    def one(b, k=None):
+        x = _Batch(b, dev, k)
+        x.plan()
+        x.select()
+        torch.cuda.synchronize()
+        stt = x.core.status()
+        if stt != 0:
+            raise RuntimeError(f"{b.name} k={x.b.k}: device status {stt}: {Bd.status_str(stt)}")
+        x.capture()
+        _time(x.g_step.replay, 3, flush)
+        return _time(x.g_step.replay, n_calls, flush)
+
+    res = {}
+    for name, b in (("pr1", W.pr1()), ("mixed_decode", W.mixed_decode())):
+        med, pr = _stats_us(one(b))
+        res[name] = {"rows": b.rows, "k": b.k, "us_per_call": med, "p10_p90": pr,
+                     "rows_per_s": round(b.rows / (med / 1e6), 1)}
+    adv = W.adversarial()
+    for k in W.ADV_KS:
+        med, pr = _stats_us(one(adv, k))
+        res[f"adversarial_k{k}"] = {"rows": adv.rows, "k": k, "us_per_call": med, "p10_p90": pr,
+                                    "rows_per_s": round(adv.rows / (med / 1e6), 1)}
+    tiny = W.tiny_rows()
+    tot_us, n_rows = 0.0, 0
+    for b in tiny:
+        med, _ = _stats_us(one(b))
+        tot_us += med
+        n_rows += b.rows
+    res["tiny_rows"] = {"rows": n_rows, "calls": len(tiny), "k": "1..16, one call per k",
+                        "us_all_calls": round(tot_us, 2),
+                        "rows_per_s": round(n_rows / (tot_us / 1e6), 1)}
+    return res
+
+
 def _cpu_baseline(b, budget_s=10.0):
     import oracle
     cores = os.cpu_count() or 1
@@ -325,10 +375,20 @@ def _cpu_baseline(b, budget_s=10.0):
             break
     dt = time.perf_counter() - t0
     score_bytes = 4 * int(b.lens.astype(np.int64).sum())
+    n1, t1 = 0, time.perf_counter()
+    while True:  # the same calls on one thread, half the budget
+        oracle.topk_batch(b, threads=1)
+        n1 += 1
+        if time.perf_counter() - t1 >= budget_s / 2:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(score_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
             "kind": "oracle",
             "sample": f"{n} full calls of {b.name} ({b.rows} rows, k={b.k}) in {dt:.1f} s, "
-                      f"rows split over {threads} threads; {dt / n * 1e6:.0f} us/call"}
+                      f"rows split over {threads} threads; {dt / n * 1e6:.0f} us/call",
+            "one_thread": {"us_per_call": round(dt1 / n1 * 1e6, 1), "calls": n1,
+                           "value": round(score_bytes * n1 / dt1 / 1e9, 4)},
+            "host_cores": cores}
 
 
 def run_reference(args):
@@ -430,6 +490,7 @@ def run_ours(args):
     sel80 = _time(bt80.g_select.replay, nsec, flush)
     e_step = _time(lambda: (bt.plan(), bt.select()), min(nsec, 100), flush)
     e_step80 = _time(lambda: (bt80.plan(), bt80.select()), min(nsec, 100), flush)
+    cfg_times = _time_configs(dev, flush, max(10, min(nsec, 50)))
     w_sel = _time(bt.g_select.replay, min(nsec, 100), None)
     w_sel80 = _time(bt80.g_select.replay, min(nsec, 100), None)
 
@@ -534,16 +595,23 @@ def run_ours(args):
             "verify_1m_select": round(sel_avg_ms * 1e3, 2),
             "verify_1m_select_p10_p90": [round(float(np.percentile(sel_ms, 10)) * 1e3, 2),
                                          round(float(np.percentile(sel_ms, 90)) * 1e3, 2)],
+            "verify_1m_select_median": _stats_us(sel_ms)[0],
+            "verify_1m_plan_select_median_p10_p90": list(_stats_us(step_ms)),
             "verify_80k_plan_select": round(float(np.mean(s80)) * 1e3, 2),
             "verify_80k_select": round(float(np.mean(sel80)) * 1e3, 2),
             "verify_80k_select_p10_p90": [round(float(np.percentile(sel80, 10)) * 1e3, 2),
                                           round(float(np.percentile(sel80, 90)) * 1e3, 2)],
+            "verify_80k_select_median": _stats_us(sel80)[0],
+            "verify_80k_plan_select_median_p10_p90": list(_stats_us(s80)),
             "verify_1m_select_warm_l2": round(float(np.mean(w_sel)) * 1e3, 2),
             "verify_80k_select_warm_l2": round(float(np.mean(w_sel80)) * 1e3, 2),
             "verify_1m_plan_select_eager": round(float(np.mean(e_step)) * 1e3, 2),
             "verify_80k_plan_select_eager": round(float(np.mean(e_step80)) * 1e3, 2),
             "pages_topk_v2": {"80k": PAGES_80K_US, "1m": PAGES_1M_US},
         },
+        "configs": dict(note="plan + select (one CUDA graph per call), L2 flushed before each "
+                             "call; median and [p10, p90] us per call; device status checked",
+                        **cfg_times),
         "key_prologue": {
             "workload": "indexer key path, 4 requests in one call: prefill chunks of 32768 "
                         "tokens at position 0, 16384 at 40000 and 16384 at 70000, one decode "
