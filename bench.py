@@ -298,20 +298,41 @@ class _Resolver:
         self.hs.copy_(self.saved[2])
 
 
-def _time(fn, steps, flush):
-    """Per-step CUDA-event times (ms) of fn(), L2 flushed before each (outside the events)."""
+RETIMED = []  # loops timed again because a host stall landed inside an event pair
+
+
+def _time_once(fn, steps, flush):
+    import gc
     import torch
     st = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
-    for i in range(steps):
-        if flush is not None:
-            flush(i)
-        ev[i][0].record(st)
-        fn()
-        ev[i][1].record(st)
-    torch.cuda.synchronize()
+    gc_was = gc.isenabled()
+    gc.disable()  # a collection between an event and its launch would be timed
+    try:
+        for i in range(steps):
+            if flush is not None:
+                flush(i)
+            ev[i][0].record(st)
+            fn()
+            ev[i][1].record(st)
+        torch.cuda.synchronize()
+    finally:
+        if gc_was:
+            gc.enable()
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def _time(fn, steps, flush, label=None):
+    """Per-step CUDA-event times (ms) of fn(), L2 flushed before each (outside the events).
+    The host enqueues each step's events around its launch; when the host stalls between
+    the two (far longer than the queued work), the stall is timed. A loop whose mean is
+    above 1.5 x its median is timed once more, and the label is recorded in RETIMED."""
+    ms = _time_once(fn, steps, flush)
+    if label is not None and steps >= 10 and np.mean(ms) > 1.5 * np.median(ms):
+        RETIMED.append(label)
+        ms = _time_once(fn, steps, flush)
+    return ms
 
 
 def _stats_us(ms):
@@ -467,7 +488,7 @@ def run_ours(args):
     if sampler:
         sampler.start()
     wall0 = time.perf_counter()
-    step_ms = _time(bt.g_step.replay, args.steps, flush)
+    step_ms = _time(bt.g_step.replay, args.steps, flush, "verify_1m_plan_select")
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
@@ -479,15 +500,15 @@ def run_ours(args):
     value = job_throughput_gbs(n, score_bytes, args.steps, total_ms)
     ms_step = total_ms / args.steps
     nsec = min(args.steps, 300)
-    sel_ms = _time(bt.g_select.replay, nsec, flush)
+    sel_ms = _time(bt.g_select.replay, nsec, flush, "verify_1m_select")
     sel_avg_ms = float(np.mean(sel_ms))
     alg_bytes = b1m.algorithmic_bytes()
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (sel_avg_ms / 1e3) / 1e9
 
     # secondary: 80K ISL latency (graph replay), eager calls, warm L2
-    s80 = _time(bt80.g_step.replay, nsec, flush)
-    sel80 = _time(bt80.g_select.replay, nsec, flush)
+    s80 = _time(bt80.g_step.replay, nsec, flush, "verify_80k_plan_select")
+    sel80 = _time(bt80.g_select.replay, nsec, flush, "verify_80k_select")
     e_step = _time(lambda: (bt.plan(), bt.select()), min(nsec, 100), flush)
     e_step80 = _time(lambda: (bt80.plan(), bt80.select()), min(nsec, 100), flush)
     cfg_times = _time_configs(dev, flush, max(10, min(nsec, 50)))
@@ -608,6 +629,7 @@ def run_ours(args):
             "verify_1m_plan_select_eager": round(float(np.mean(e_step)) * 1e3, 2),
             "verify_80k_plan_select_eager": round(float(np.mean(e_step80)) * 1e3, 2),
             "pages_topk_v2": {"80k": PAGES_80K_US, "1m": PAGES_1M_US},
+            "retimed": list(RETIMED),
         },
         "configs": dict(note="plan + select (one CUDA graph per call), L2 flushed before each "
                              "call; median and [p10, p90] us per call; device status checked",

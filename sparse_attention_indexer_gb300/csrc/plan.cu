@@ -273,16 +273,26 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
         x.pad = 0;
         ri[lane] = x;
       }
-      // single rows: longest length bucket first, row order inside a bucket
+      // single rows: longest length bucket first, row order inside a bucket. A lane's
+      // rank counts the single rows of a larger bucket and those of its bucket in lower
+      // lanes: the 5-bit buckets are compared bit by bit from the top on ballots.
       const bool single = lane < rows && !multi;
       const int bucket = L > 0 ? 31 - __clz(L) : 0;
-      int rank = 0;
-      for (int j = 0; j < 32; ++j) {
-        const int bj = __shfl_sync(kAll, bucket, j);
-        const bool sj = __shfl_sync(kAll, single ? 1 : 0, j) != 0;
-        rank += (sj && (bj > bucket || (bj == bucket && j < lane))) ? 1 : 0;
+      const unsigned sm = __ballot_sync(kAll, single);
+      unsigned eq = sm, gt = 0u;
+#pragma unroll
+      for (int bit = 4; bit >= 0; --bit) {
+        const bool one = (bucket >> bit) & 1;
+        const unsigned ones = __ballot_sync(kAll, single && one);
+        if (one) {
+          eq &= ones;
+        } else {
+          gt |= eq & ones;
+          eq &= ~ones;
+        }
       }
-      const int n_single = __popc(__ballot_sync(kAll, single));
+      const int rank = __popc(gt) + __popc(eq & lt);
+      const int n_single = __popc(sm);
       if (single) singles[rank] = make_int2(lane, Lraw);
       const int n_multi = __popc(mm);
       if (lane == 0) {
@@ -310,11 +320,9 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
   __syncthreads();
   if (!s.bcast[4]) return false;
   const int n_multi = s.bcast[0], total_slots = s.bcast[1], n_single = s.bcast[2];
-  // Unit table of wave 0 for the grid's CTAs (two threads per descriptor, 16 bytes
-  // each: each warp stores 512 contiguous bytes); the first-single table in closed
-  // form (busy CTAs are [0, total_slots)).
-  for (int i = tid; i < 2 * grid; i += kPlanThreads) {
-    const int b = i >> 1;
+  // Unit table of wave 0 (one thread per CTA, its descriptor as two 16-byte stores)
+  // and the first-single table in closed form (busy CTAs are [0, total_slots)).
+  for (int b = tid; b < grid; b += kPlanThreads) {
     UnitDesc u{-1, 0, 0, 0, 0, 0, 0, 0};
     if (n_multi > 0 && b < total_slots) {
       int lo = 0, hi = n_multi - 1;  // last group whose first CTA <= b
@@ -326,12 +334,11 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
       const int row = s.multi_rows[lo];
       u = make_unit(row, s.lens[row], b - s.multi_cta[lo], s.multi_g[lo], lo);
     }
-    const uint4 half = (i & 1) ? make_uint4(u.rank, u.G, u.group, u.pad)
-                               : make_uint4(u.row, u.s0, u.n, u.len);
-    reinterpret_cast<uint4*>(units + b)[i & 1] = half;
-  }
-  for (int b = tid; b < grid; b += kPlanThreads)
+    uint4* d = reinterpret_cast<uint4*>(units + b);
+    d[0] = make_uint4(u.row, u.s0, u.n, u.len);
+    d[1] = make_uint4(u.rank, u.G, u.group, u.pad);
     first_single[b] = (b >= total_slots && b - total_slots < n_single) ? b - total_slots : -1;
+  }
   return true;
 }
 

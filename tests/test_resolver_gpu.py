@@ -155,3 +155,16 @@ def test_victims_from_slots_last_used_over_many_steps(n_miss, never_used):
     state = _crafted_state(b, 40, 40, n_miss, 200, W.SEED_BASE + 77 + n_miss, never_used)
     counts = _one_step_from(b, state, 40)
     assert np.all(counts[:, 2] == n_miss) and np.all(counts[:, 1] == 200)
+
+
+@pytest.mark.parametrize("n_miss,never_used", [(150, 0.0), (700, 0.0)])
+def test_victims_in_a_hot_buffer_of_odd_size(n_miss, never_used):
+    """1000 slots per request (the last thread's block of 8 slots is partly outside):
+    150 misses take slots from the oldest few steps, 700 reach far younger ones."""
+    import dataclasses
+    b = W.hisparse(seed=W.SEED_BASE + 78, reqs=2, k=1024, lens=[50000, 20000], row_bytes=48,
+                   n_steps=1)
+    b = dataclasses.replace(b, hot_rows=np.ascontiguousarray(b.hot_rows[:, :1000]))
+    state = _crafted_state(b, 30, 30, n_miss, 100, W.SEED_BASE + 79 + n_miss, never_used)
+    counts = _one_step_from(b, state, 30)
+    assert np.all(counts[:, 2] == n_miss) and np.all(counts[:, 1] == 100)
