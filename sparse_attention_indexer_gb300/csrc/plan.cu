@@ -212,7 +212,11 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
     const int Lraw = lane < rows ? lens[lane] : 0;
     const int L = lane < rows ? valid_len(Lraw, max_len) : 0;
     long long tot = L;
-    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(kAll, tot, o);
+    int mx = L;
+    for (int o = 16; o; o >>= 1) {
+      tot += __shfl_xor_sync(kAll, tot, o);
+      mx = max(mx, __shfl_xor_sync(kAll, mx, o));
+    }
     // CTAs of the split rows at chunk cc (every lane evaluates its own cc)
     auto slots_at = [&](int cc) {
       const Divider dv(cc);
@@ -225,11 +229,18 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
     };
     if (lane < rows) s.lens[lane] = L;
     const int c0 = initial_chunk(tot, grid, 0);
-    // a fails (c0 may pass); b = kChunkCap passes unless no chunk fits, which the
-    // first round (lane 31 evaluates b) shows
+    // a fails (c0 may pass). b: with grid / rows CTAs for every row, chunk
+    // ceil(max length / (grid / rows)) fits whatever the lengths, so b is that chunk
+    // (at least c0) when it is below kChunkCap; else kChunkCap, which passes unless no
+    // chunk fits. The first round always runs, and its lane 31 evaluates b.
     int a = c0 - kChunkAlign, b = kChunkCap;
+    const int per_row = rows > 0 ? grid / rows : 0;
+    if (per_row > 0) {
+      const uint32_t hi = ((uint32_t)mx + (uint32_t)per_row - 1u) / (uint32_t)per_row;
+      if (hi < (uint32_t)kChunkCap) b = max(c0, round_chunk(hi));
+    }
     bool fits = true;
-    while (b - a > kChunkAlign) {
+    do {
       int step = (b - a + 31) / 32;
       step = (step + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
       const int cand = min(a + step * (lane + 1), b);
@@ -243,7 +254,7 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
       const int na = __shfl_sync(kAll, cand, max(first - 1, 0));
       a = first == 0 ? a : na;
       b = nb;
-    }
+    } while (b - a > kChunkAlign);
     const int c = b;
     if (lane == 0) s.bcast[4] = fits ? 1 : 0;
     if (fits) {

@@ -212,7 +212,13 @@ def test_device_plan_matches_host_reference():
     grid = B.topk_grid_size()
     mixed = W.mixed_decode()
     few = _subset(mixed, np.arange(20))  # <= 32 rows: the one-warp planner, both row kinds
-    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few):
+    # lengths alone (the plan reads nothing else): more than grid * 48128 values over
+    # <= 32 rows start the search at the chunk cap, where nothing fits one wave
+    import types
+    big = [types.SimpleNamespace(lens=np.array(l, np.int32), rows=len(l), max_len=max(l))
+           for l in ([1_000_000] * 8, [300_000] * 32, [1_900_000] * 4, [7_000_000, 10],
+                     [48_128 * 21] * 7, [48_127] * 32)]
+    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, *big):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
@@ -329,3 +335,17 @@ def test_skewed_rows_over_many_ctas():
         slots, pos, st = run_gpu(one, k=k, chunk=48128)
         assert st == 0
         compare_with_oracle(one, k, slots, pos)
+
+
+def test_eight_rows_of_1m_take_two_waves():
+    """8 rows x 1,000,000: 168 CTAs at the largest chunk, more than one wave of the grid
+    (the small-batch planner must hand these rows to the multi-wave path)."""
+    rng = np.random.default_rng(W.SEED_BASE + 40)
+    L = 1_000_000
+    s = rng.standard_normal((8, L)).astype(np.float32)
+    tab = rng.permutation(L // 64 + 1).astype(np.int32)[None, :]
+    b = W.Batch("eight_1m", s, np.full(8, L, np.int32), L, 2048, tab,
+                np.zeros(8, np.int32), 64)
+    slots, pos, st = run_gpu(b)
+    assert st == 0, B.status_str(st)
+    compare_with_oracle(b, b.k, slots, pos)
