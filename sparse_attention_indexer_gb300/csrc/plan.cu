@@ -241,9 +241,19 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
     }
     bool fits = true;
     do {
-      int step = (b - a + 31) / 32;
-      step = (step + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
-      const int cand = min(a + step * (lane + 1), b);
+      // 32 increasing candidates in (a, b], b among them. A wide bracket gets 16 spread
+      // over (a, b - 256] and 16 at steps of 16 up to b: equal lengths put the answer
+      // at or just below b, which one round then settles.
+      int cand;
+      if (b - a <= 32 * kChunkAlign) {
+        cand = min(a + kChunkAlign * (lane + 1), b);
+      } else if (lane >= 16) {
+        cand = b - kChunkAlign * (31 - lane);
+      } else {
+        int step = (b - 16 * kChunkAlign - a + 15) / 16;
+        step = (step + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+        cand = min(a + step * (lane + 1), b - 16 * kChunkAlign);
+      }
       const unsigned m = __ballot_sync(kAll, slots_at(cand) <= grid);
       if (m == 0u) {
         fits = false;
