@@ -402,8 +402,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
   // Lengths are read many times below: keep them in shared memory when they fit.
   const bool cached = rows <= kLensCache;
-  if (cached)
-    for (int r = tid; r < rows; r += kPlanThreads) s.lens[r] = lens[r];
+  if (cached) {
+    // eight independent loads per thread in flight: the lengths come from cold memory
+    for (int r0 = 0; r0 < rows; r0 += 8 * kPlanThreads) {
+      int v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e * kPlanThreads + tid;
+        v[e] = r < rows ? lens[r] : 0;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e * kPlanThreads + tid;
+        if (r < rows) s.lens[r] = v[e];
+      }
+    }
+  }
   __syncthreads();
   const int32_t* L_ = cached ? s.lens : lens;
 
@@ -422,25 +436,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   int waves = 0, plan_error = 0, n_multi = 0;
   if (!forced && fits) {
     // One wave: a row's group index and first CTA are exclusive prefixes over the
-    // rows (at most grid CTAs in total, so both fit 16 bits).
+    // rows (at most grid CTAs in total, so both fit 16 bits). Thread t takes a
+    // contiguous range of rows, so one block scan of its (count, CTAs) orders them.
     const Divider dv(c);
-    int base_n = 0, base_g = 0;
-    for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
-      const int r = r0 + tid;
-      const int G = r < rows ? dv.groups(valid_len(L_[r], max_len)) : 1;
-      int tot;
-      const int off = block_scan(G > 1 ? ((1 << 16) | G) : 0, &tot, s);
+    const int per = (rows + kPlanThreads - 1) / kPlanThreads;
+    const int rb = min(rows, tid * per), re = min(rows, rb + per);
+    int mine = 0;
+    for (int r = rb; r < re; ++r) {
+      const int G = dv.groups(valid_len(L_[r], max_len));
+      if (G > 1) mine += (1 << 16) | G;
+    }
+    int tot;
+    int off = block_scan(mine, &tot, s);
+    for (int r = rb; r < re && mine; ++r) {
+      const int G = dv.groups(valid_len(L_[r], max_len));
       if (G > 1) {
-        const int i = base_n + (off >> 16);
+        const int i = off >> 16;
         s.multi_rows[i] = r;
         s.multi_g[i] = G;
         s.multi_wave[i] = 0;
-        s.multi_cta[i] = base_g + (off & 0xFFFF);
+        s.multi_cta[i] = off & 0xFFFF;
+        off += (1 << 16) | G;
       }
-      base_n += tot >> 16;
-      base_g += tot & 0xFFFF;
     }
-    n_multi = base_n;
+    n_multi = tot >> 16;
     waves = n_multi > 0 ? 1 : 0;
   } else {
     // Forced chunk, or rows that do not fit one wave even at kChunkCap: grow the
@@ -547,9 +566,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   // Single-CTA rows, longest bucket first, row order inside a bucket.
   if (tid == 0) s.bucket_mask = 0u;
   __syncthreads();
-  for (int r = tid; r < rows; r += kPlanThreads) {
-    const int L = valid_len(L_[r], max_len);
-    if (plan_error || dvc.groups(L) == 1) atomicOr(&s.bucket_mask, 1u << len_bucket(L));
+  {
+    // each thread ORs its rows' buckets, a warp reduction, one shared atomic per warp
+    unsigned bm = 0u;
+    for (int r = tid; r < rows; r += kPlanThreads) {
+      const int L = valid_len(L_[r], max_len);
+      if (plan_error || dvc.groups(L) == 1) bm |= 1u << len_bucket(L);
+    }
+    bm = __reduce_or_sync(0xffffffffu, bm);
+    if ((tid & 31) == 0 && bm) atomicOr(&s.bucket_mask, bm);
   }
   __syncthreads();
   TOPK_MARK(g_plan_trace, 7);
@@ -558,22 +583,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 #endif
   const unsigned mask = s.bucket_mask;
   int n_single = 0;
+  {
+    // thread t takes a contiguous range of rows: one block scan per present bucket
+    const int per = (rows + kPlanThreads - 1) / kPlanThreads;
+    const int rb = min(rows, tid * per), re = min(rows, rb + per);
 #pragma unroll 1
-  for (unsigned m = mask; m != 0u; m &= ~(1u << (31 - __clz(m)))) {
-    const int b = 31 - __clz(m);  // present buckets, longest first
-#pragma unroll 1
-    for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {
-      const int r = r0 + tid;
-      bool take = false;
-      int Lraw = 0;
-      if (r < rows) {
-        Lraw = L_[r];
-        const int L = valid_len(Lraw, max_len);
-        take = (plan_error || dvc.groups(L) == 1) && len_bucket(L) == b;
+    for (unsigned m = mask; m != 0u; m &= ~(1u << (31 - __clz(m)))) {
+      const int b = 31 - __clz(m);  // present buckets, longest first
+      int cnt = 0;
+      for (int r = rb; r < re; ++r) {
+        const int L = valid_len(L_[r], max_len);
+        cnt += ((plan_error || dvc.groups(L) == 1) && len_bucket(L) == b) ? 1 : 0;
       }
       int tot;
-      const int off = block_scan(take ? 1 : 0, &tot, s);
-      if (take) singles[n_single + off] = make_int2(r, Lraw);
+      int off = n_single + block_scan(cnt, &tot, s);
+      for (int r = rb; r < re && cnt; ++r) {
+        const int Lraw = L_[r];
+        const int L = valid_len(Lraw, max_len);
+        if ((plan_error || dvc.groups(L) == 1) && len_bucket(L) == b) {
+          singles[off++] = make_int2(r, Lraw);
+          --cnt;
+        }
+      }
       n_single += tot;
     }
   }

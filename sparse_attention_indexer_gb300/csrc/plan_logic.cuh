@@ -110,12 +110,16 @@ inline bool auto_chunk_ref(int c0, int grid, SlotsAt slots_at, int* c) {
 
 // Bucket of a single-CTA row for the longest-first claim order.
 __host__ __device__ inline int len_bucket(int L) {
+#ifdef __CUDA_ARCH__
+  return L > 1 ? 31 - __clz(L) : 0;  // floor(log2 L): the loop below, without the loop
+#else
   int b = 0;
   while (L > 1 && b < 31) {
     L >>= 1;
     ++b;
   }
   return b;
+#endif
 }
 
 // The unit of chunk `rank` of a row split over G CTAs.

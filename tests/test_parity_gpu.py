@@ -218,7 +218,8 @@ def test_device_plan_matches_host_reference():
     big = [types.SimpleNamespace(lens=np.array(l, np.int32), rows=len(l), max_len=max(l))
            for l in ([1_000_000] * 8, [300_000] * 32, [1_900_000] * 4, [7_000_000, 10],
                      [48_128 * 21] * 7, [48_127] * 32)]
-    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, *big):
+    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, W.prefill(),
+              *big):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
