@@ -191,13 +191,14 @@ __device__ int auto_chunk(const int32_t* L_, int rows, int max_len, int grid, lo
   return hi;
 }
 
-// Plan of a batch of at most 32 rows without a forced chunk: warp 0 decides (lane =
-// row: the chunk search tries 32 candidates per round, a ballot picks the first that
-// fits; group indices and first CTAs are warp scans), then the block writes the
-// tables. Same plan as the general path below (auto_chunk_ref's rule, one wave).
+// Plan of a batch of at most 64 rows without a forced chunk: warp 0 decides (lane l
+// holds rows l and l + 32: the chunk search tries 32 candidates per round, a ballot
+// picks the first that fits; group indices and first CTAs are warp scans), then the
+// block writes the tables. Same plan as the general path below (auto_chunk_ref's rule, one wave).
 // Returns false, with nothing written, when the rows do not fit one wave even at
 // kChunkCap (the general path then packs several waves).
-constexpr int kSmallRows = 32;
+constexpr int kSmallRows = 64;
+constexpr int kRowsPerLane = kSmallRows / 32;  // lane l holds rows l and l + 32
 
 __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_len, int grid,
                            char* ws, const Layout& lay, PlanSmem& s) {
@@ -208,11 +209,22 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
   UnitDesc* units = reinterpret_cast<UnitDesc*>(ws + lay.units);
   const int tid = threadIdx.x, lane = tid & 31;
   constexpr unsigned kAll = 0xffffffffu;
+  constexpr int kR = kRowsPerLane;
   if (tid < 32) {
-    const int Lraw = lane < rows ? lens[lane] : 0;
-    const int L = lane < rows ? valid_len(Lraw, max_len) : 0;
-    long long tot = L;
-    int mx = L;
+    int Lraw[kR], L[kR];
+#pragma unroll
+    for (int q = 0; q < kR; ++q) {
+      const int r = lane + 32 * q;
+      Lraw[q] = r < rows ? lens[r] : 0;
+      L[q] = r < rows ? valid_len(Lraw[q], max_len) : 0;
+    }
+    long long tot = 0;
+    int mx = 0;
+#pragma unroll
+    for (int q = 0; q < kR; ++q) {
+      tot += L[q];
+      mx = max(mx, L[q]);
+    }
     for (int o = 16; o; o >>= 1) {
       tot += __shfl_xor_sync(kAll, tot, o);
       mx = max(mx, __shfl_xor_sync(kAll, mx, o));
@@ -221,13 +233,17 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
     auto slots_at = [&](int cc) {
       const Divider dv(cc);
       int n = 0;
-      for (int r = 0; r < rows; ++r) {
-        const int G = dv.groups(__shfl_sync(kAll, L, r));
-        n += G > 1 ? G : 0;
-      }
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        for (int j = 0; j < 32 && 32 * q + j < rows; ++j) {
+          const int G = dv.groups(__shfl_sync(kAll, L[q], j));
+          n += G > 1 ? G : 0;
+        }
       return n;
     };
-    if (lane < rows) s.lens[lane] = L;
+#pragma unroll
+    for (int q = 0; q < kR; ++q)
+      if (lane + 32 * q < rows) s.lens[lane + 32 * q] = L[q];
     const int c0 = initial_chunk(tot, grid, 0);
     // a fails (c0 may pass). b: with grid / rows CTAs for every row, chunk
     // ceil(max length / (grid / rows)) fits whatever the lengths, so b is that chunk
@@ -268,54 +284,81 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
     const int c = b;
     if (lane == 0) s.bcast[4] = fits ? 1 : 0;
     if (fits) {
+      // Rows in row order: all of the first set (lanes' rows 0..31), then the second.
       const Divider dv(c);
-      const int G = lane < rows ? dv.groups(L) : 1;
-      const bool multi = G > 1;
       const unsigned lt = (1u << lane) - 1u;
-      const unsigned mm = __ballot_sync(kAll, multi);
-      const int gi = __popc(mm & lt);
-      int incl = multi ? G : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kAll, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int total_slots = __shfl_sync(kAll, incl, 31);
-      if (multi) {
-        s.multi_rows[gi] = lane;
-        s.multi_g[gi] = G;
-        s.multi_wave[gi] = 0;
-        s.multi_cta[gi] = incl - G;
-      }
-      if (lane < rows) {
-        RowInfo x;
-        x.len = Lraw;
-        x.G = G;
-        x.group = multi ? gi : -1;
-        x.pad = 0;
-        ri[lane] = x;
-      }
-      // single rows: longest length bucket first, row order inside a bucket. A lane's
-      // rank counts the single rows of a larger bucket and those of its bucket in lower
-      // lanes: the 5-bit buckets are compared bit by bit from the top on ballots.
-      const bool single = lane < rows && !multi;
-      const int bucket = L > 0 ? 31 - __clz(L) : 0;
-      const unsigned sm = __ballot_sync(kAll, single);
-      unsigned eq = sm, gt = 0u;
+      int G[kR], gi[kR];
+      bool multi[kR], single[kR];
+      unsigned mm[kR], sm[kR];
+      int bucket[kR];
+      int before_m = 0, before_g = 0;  // multi rows and their CTAs in the earlier sets
 #pragma unroll
-      for (int bit = 4; bit >= 0; --bit) {
-        const bool one = (bucket >> bit) & 1;
-        const unsigned ones = __ballot_sync(kAll, single && one);
-        if (one) {
-          eq &= ones;
-        } else {
-          gt |= eq & ones;
-          eq &= ~ones;
+      for (int q = 0; q < kR; ++q) {
+        const int r = lane + 32 * q;
+        G[q] = r < rows ? dv.groups(L[q]) : 1;
+        multi[q] = G[q] > 1;
+        mm[q] = __ballot_sync(kAll, multi[q]);
+        gi[q] = before_m + __popc(mm[q] & lt);
+        int incl = multi[q] ? G[q] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kAll, incl, o);
+          if (lane >= o) incl += y;
         }
+        if (multi[q]) {
+          s.multi_rows[gi[q]] = r;
+          s.multi_g[gi[q]] = G[q];
+          s.multi_wave[gi[q]] = 0;
+          s.multi_cta[gi[q]] = before_g + incl - G[q];
+        }
+        if (r < rows) {
+          RowInfo x;
+          x.len = Lraw[q];
+          x.G = G[q];
+          x.group = multi[q] ? gi[q] : -1;
+          x.pad = 0;
+          ri[r] = x;
+        }
+        before_m += __popc(mm[q]);
+        before_g += __shfl_sync(kAll, incl, 31);
+        single[q] = r < rows && !multi[q];
+        bucket[q] = L[q] > 0 ? 31 - __clz(L[q]) : 0;
+        sm[q] = __ballot_sync(kAll, single[q]);
       }
-      const int rank = __popc(gt) + __popc(eq & lt);
-      const int n_single = __popc(sm);
-      if (single) singles[rank] = make_int2(lane, Lraw);
-      const int n_multi = __popc(mm);
+      const int total_slots = before_g;
+      // single rows: longest length bucket first, row order inside a bucket. A row's
+      // rank counts the single rows of a larger bucket and those of its bucket in lower
+      // rows: the 5-bit buckets are compared bit by bit from the top on ballots.
+      unsigned ones[kR][5];
+#pragma unroll
+      for (int p = 0; p < kR; ++p)
+#pragma unroll
+        for (int bit = 0; bit < 5; ++bit)
+          ones[p][bit] = __ballot_sync(kAll, single[p] && ((bucket[p] >> bit) & 1));
+      int n_single = 0;
+#pragma unroll
+      for (int p = 0; p < kR; ++p) n_single += __popc(sm[p]);
+#pragma unroll
+      for (int q = 0; q < kR; ++q) {
+        int rank = 0;
+#pragma unroll
+        for (int p = 0; p < kR; ++p) {
+          unsigned eq = sm[p], gt = 0u;
+#pragma unroll
+          for (int bit = 4; bit >= 0; --bit) {
+            if ((bucket[q] >> bit) & 1) {
+              eq &= ones[p][bit];
+            } else {
+              gt |= eq & ones[p][bit];
+              eq &= ~ones[p][bit];
+            }
+          }
+          rank += __popc(gt) + (p < q ? __popc(eq) : p == q ? __popc(eq & lt) : 0);
+        }
+        if (single[q]) singles[rank] = make_int2(lane + 32 * q, Lraw[q]);
+      }
+      int n_multi = 0;
+#pragma unroll
+      for (int q = 0; q < kR; ++q) n_multi += __popc(mm[q]);
       if (lane == 0) {
         const int n_implicit = min(grid - total_slots, n_single);
         h->magic = kMagic;

@@ -211,15 +211,17 @@ def test_device_plan_matches_host_reference():
     from tests.test_plan_host import parse_plan
     grid = B.topk_grid_size()
     mixed = W.mixed_decode()
-    few = _subset(mixed, np.arange(20))  # <= 32 rows: the one-warp planner, both row kinds
+    few = _subset(mixed, np.arange(20))   # one-warp planner, one row per lane, both row kinds
+    more = _subset(mixed, np.arange(45))  # one-warp planner, rows 32.. in each lane's second row
     # lengths alone (the plan reads nothing else): more than grid * 48128 values over
-    # <= 32 rows start the search at the chunk cap, where nothing fits one wave
+    # <= 64 rows start the search at the chunk cap, where nothing fits one wave
     import types
     big = [types.SimpleNamespace(lens=np.array(l, np.int32), rows=len(l), max_len=max(l))
            for l in ([1_000_000] * 8, [300_000] * 32, [1_900_000] * 4, [7_000_000, 10],
-                     [48_128 * 21] * 7, [48_127] * 32)]
-    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, W.prefill(),
-              *big):
+                     [48_128 * 21] * 7, [48_127] * 32, [200_000] * 50, [48_127] * 64,
+                     [3000 + 977 * i for i in range(63)])]
+    for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, more,
+              W.tiny_rows()[0], W.tiny_rows()[15], W.prefill(), *big):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
