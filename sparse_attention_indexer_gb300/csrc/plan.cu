@@ -42,6 +42,9 @@ struct PlanSmem {
   int32_t multi_cta[kMaxGroups];
   uint8_t busy[kMaxGrid];  // CTAs with static units
   unsigned bucket_mask;
+  int32_t wcnt[kPlanWarps][32];  // one-pass ranking: a round's single rows per warp, bucket
+  int32_t bbase[32];             // first rank of each bucket (longer buckets first)
+  int32_t bcarry[32];            // single rows of each bucket in the earlier rounds
   int32_t lens[kLensCache];
 };
 
@@ -626,7 +629,71 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 #endif
   const unsigned mask = s.bucket_mask;
   int n_single = 0;
-  {
+  const int rounds = (rows + kPlanThreads - 1) / kPlanThreads;
+  if (__popc(mask) > 2 * rounds) {
+    // Many buckets, few rows: one pass in rounds of kPlanThreads rows (row r0 + tid).
+    // A row's rank is its bucket's first rank, plus the bucket's single rows in earlier
+    // rounds, in lower warps of this round and in lower lanes of its warp (peers by
+    // __match_any_sync on the bucket). Two sweeps: bucket totals, then the ranks.
+    const int lane = tid & 31, w = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    if (tid < 32) {
+      s.bbase[tid] = 0;
+      s.bcarry[tid] = 0;
+    }
+    __syncthreads();
+    for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {  // totals per bucket
+      const int r = r0 + tid;
+      int key = 64 + lane;  // unique: matches no bucket
+      if (r < rows) {
+        const int L = valid_len(L_[r], max_len);
+        if (plan_error || dvc.groups(L) == 1) key = len_bucket(L);
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key < 32 && (peers & lt) == 0u) atomicAdd(&s.bbase[key], __popc(peers));
+    }
+    __syncthreads();
+    if (tid < 32) {  // bbase[b] := single rows in buckets above b (longer first)
+      const int t = s.bbase[tid];
+      int incl = t;  // inclusive suffix sum: buckets >= tid
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      s.bbase[tid] = incl - t;
+      if (tid == 0) s.bcast[5] = incl;  // all single rows
+    }
+    __syncthreads();
+    n_single = s.bcast[5];
+    for (int r0 = 0; r0 < rows; r0 += kPlanThreads) {  // ranks
+      const int r = r0 + tid;
+      int key = 64 + lane, Lraw = 0;
+      if (r < rows) {
+        Lraw = L_[r];
+        const int L = valid_len(Lraw, max_len);
+        if (plan_error || dvc.groups(L) == 1) key = len_bucket(L);
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      s.wcnt[w][lane] = 0;
+      __syncwarp();
+      if (key < 32 && (peers & lt) == 0u) s.wcnt[w][key] = __popc(peers);
+      __syncthreads();
+      if (key < 32) {
+        int rank = s.bbase[key] + s.bcarry[key] + __popc(peers & lt);
+        for (int v = 0; v < w; ++v) rank += s.wcnt[v][key];
+        singles[rank] = make_int2(r, Lraw);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        int add = 0;
+#pragma unroll
+        for (int v = 0; v < kPlanWarps; ++v) add += s.wcnt[v][tid];
+        s.bcarry[tid] += add;
+      }
+      __syncthreads();
+    }
+  } else {
     // thread t takes a contiguous range of rows: one block scan per present bucket
     const int per = (rows + kPlanThreads - 1) / kPlanThreads;
     const int rb = min(rows, tid * per), re = min(rows, rb + per);
