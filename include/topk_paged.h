@@ -135,6 +135,20 @@ const char* topk_status_str(int code);
 /* Number of CTAs of the persistent select grid on the current device. */
 int topk_grid_size(void);
 
+/* Test entry: topk_select_paged with every bounded wait limited to `wait_ns`
+ * nanoseconds (0 = the default 200 ms) and CTA `skip_cta` (>= 0; -1 = none) never
+ * arriving at the first row barrier of its multi-CTA units: the other CTAs of that row
+ * then give up after `wait_ns`, the call ends, TOPK_STATUS_TIMEOUT is set and the first
+ * expired wait is recorded in the workspace header (bytes 128..159: kind (1 = row
+ * barrier, 2 = piece copy), row, rank, barrier sequence, stuck rank, target, CTA).
+ * Rows served by other CTAs are unaffected. Used to test that expired waits end the
+ * call cleanly; after it, call topk_plan again. */
+int topk_select_paged_test(const float* scores, int64_t ld, const int32_t* lens, int rows,
+                           int max_len, int k, const int32_t* block_table, int64_t table_ld,
+                           const int32_t* row_to_table, int page_size, int32_t* out_slots,
+                           int32_t* out_pos, void* workspace, topk_stream_t stream,
+                           uint64_t wait_ns, int skip_cta);
+
 /* Limits of topk_select_paged_noalloc: its scratch is a fixed 10 MiB array in the
  * library's device image, enough for the plan and group states of 64 rows. */
 #define TOPK_STATIC_MAX_ROWS 64
@@ -155,7 +169,9 @@ int topk_grid_size(void);
  *   status      device int32 [1] or NULL: receives this call's device status bits
  *               (TOPK_STATUS_*) once the stream reaches the end of the call
  * Returns TOPK_ERR_STATIC_ROWS for rows > TOPK_STATIC_MAX_ROWS, otherwise the codes
- * of topk_plan / topk_select_paged; any negative return enqueued nothing.
+ * of topk_plan / topk_select_paged. Argument errors are found before anything is
+ * enqueued; TOPK_ERR_CUDA (a launch or copy that failed) may leave the planning
+ * kernel enqueued on the scratch array, with no select after it.
  * The first call on each device looks up the scratch array's address with
  * cudaGetSymbolAddress (with that device current) and queries the device; make that
  * first call before any stream capture begins. There is one scratch array per

@@ -10,8 +10,7 @@ LayerNorm, RoPE, FP8 quantization and the paged indexer-KV-cache store, fused in
 kernel, on the key activations that the fused wk projection produced (the projection
 itself is a GEMM, outside this step; the fused path has no Hadamard transform).
 
-The pages name the steps but fix none of their parameters. Readings taken here (each
-also listed in the design doc):
+The pages name the steps but fix none of their parameters. Readings taken here:
 
 * LayerNorm over the D channels of one token, with per-channel weight w and bias b:
   y = (x - mean) / sqrt(var + eps) * w + b, var the biased (population) variance.

@@ -11,7 +11,7 @@ hot tokens are read and their LRU entry refreshed, a miss copies a single row fr
 pinned host memory into an LRU slot) and section "Composing with the rest of vLLM"
 (hot buffers default to 2 x top-K rows per request).
 
-Readings taken here (the pages sketch the policy; each is also listed in the design doc):
+Readings taken here (the pages sketch the policy):
 
 * Request j's block table row maps page p // page_size to a physical block (>= 0,
   resident) or a null placeholder (< 0: the page lives in host memory only).

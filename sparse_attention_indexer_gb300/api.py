@@ -31,6 +31,7 @@ class PagedTopK:
         assert self.workspace.data_ptr() % 256 == 0
 
     def plan(self, lens: torch.Tensor, chunk: int = 0, stream=None) -> None:
+        """chunk forces the elements per CTA when nonzero (tests: path forcing)."""
         assert lens.dtype == torch.int32 and lens.is_cuda and lens.numel() == self.rows
         if chunk:
             B.topk_plan_ex(lens, self.rows, self.max_len, chunk, self.workspace, self.ws_bytes,

@@ -33,6 +33,7 @@ EXPORTS = (
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
     "topk_select_paged_noalloc", "indexer_k_prologue", "hisparse_resolve",
+    "topk_select_paged_test",
 )
 
 
@@ -60,6 +61,9 @@ _SIGS = {
     "topk_status_str": (_c.c_char_p, [_c.c_int]),
     "topk_plan_host": (_c.c_int, [_VP, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_size_t]),
     "topk_layout_info": (_c.c_int, [_c.c_int, _c.POINTER(_c.c_int64), _c.c_int]),
+    "topk_select_paged_test": (_c.c_int, [_VP, _c.c_int64, _VP, _c.c_int, _c.c_int, _c.c_int,
+                                          _VP, _c.c_int64, _VP, _c.c_int, _VP, _VP, _VP, _VP,
+                                          _c.c_uint64, _c.c_int]),
     "topk_select_paged_noalloc": (_c.c_int, [_VP, _c.c_int64, _VP, _c.c_int, _c.c_int, _c.c_int,
                                              _VP, _c.c_int64, _VP, _c.c_int, _VP, _VP, _VP, _VP]),
     "indexer_k_prologue": (_c.c_int, [_VP, _c.c_int64, _c.c_int, _c.c_int, _VP, _VP, _c.c_float,
@@ -168,6 +172,17 @@ def topk_plan_ex(lens, rows: int, max_len: int, chunk: int, workspace, ws_bytes:
     return _check(lib().topk_plan_ex(_ptr(lens), int(rows), int(max_len), int(chunk),
                                      _ptr(workspace), int(ws_bytes), _stream(stream)),
                   "topk_plan_ex")
+
+
+def topk_select_paged_test(scores, ld: int, lens, rows: int, max_len: int, k: int, block_table,
+                           table_ld: int, row_to_table, page_size: int, out_slots, out_pos,
+                           workspace, wait_ns: int, skip_cta: int, stream=None) -> int:
+    """topk_select_paged with a bounded-wait limit (ns) and a CTA that skips the first
+    row-barrier arrival of its units (test hooks)."""
+    return _check(lib().topk_select_paged_test(
+        _ptr(scores), int(ld), _ptr(lens), int(rows), int(max_len), int(k), _ptr(block_table),
+        int(table_ld), _ptr(row_to_table), int(page_size), _ptr(out_slots), _ptr(out_pos),
+        _ptr(workspace), _stream(stream), int(wait_ns), int(skip_cta)), "topk_select_paged_test")
 
 
 def topk_select_paged(scores, ld: int, lens, rows: int, max_len: int, k: int, block_table,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
 SOURCES = ["select.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu", "resolver.cu"]
-HEADERS = ["common.cuh", "plan_logic.cuh"]
+HEADERS = ["common.cuh", "keys.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -71,6 +71,47 @@ int plan_common(const int32_t* lens, int rows, int max_len, int chunk, void* ws,
   return TOPK_OK;
 }
 
+int select_common(const float* scores, int64_t ld, const int32_t* lens, int rows, int max_len,
+                  int k, const int32_t* block_table, int64_t table_ld,
+                  const int32_t* row_to_table, int page_size, int32_t* out_slots,
+                  int32_t* out_pos, void* workspace, cudaStream_t stream, uint64_t wait_ns,
+                  int skip_cta) {
+  if (rows < 0) return TOPK_ERR_ROWS;
+  if (k < 1 || k > TOPK_MAX_K) return TOPK_ERR_K;
+  if (page_size < 1) return TOPK_ERR_PAGE_SIZE;
+  if (max_len < 0) return TOPK_ERR_MAX_LEN;
+  if (ld < max_len || table_ld < 1) return TOPK_ERR_LD;
+  if (!workspace) return TOPK_ERR_NULL;
+  if (rows == 0) return TOPK_OK;
+  if (!scores || !lens || !block_table || !out_slots) return TOPK_ERR_NULL;
+  if (!aligned(scores, 4) || !aligned(out_slots, 4) || (out_pos && !aligned(out_pos, 4)) ||
+      !aligned(lens, 4) || !aligned(block_table, 4) || (row_to_table && !aligned(row_to_table, 4)))
+    return TOPK_ERR_ALIGN;
+  if (!aligned(workspace, 256)) return TOPK_ERR_WORKSPACE;
+  int grid = 0;
+  const int e = device_grid(&grid);
+  if (e != TOPK_OK) return e;
+  if ((int64_t)max_len > (int64_t)grid * kChunkCap) return TOPK_ERR_MAX_LEN;
+  SelectParams p;
+  p.scores = scores;
+  p.ld = ld;
+  p.lens = lens;
+  p.rows = rows;
+  p.max_len = max_len;
+  p.k = k;
+  p.table = block_table;
+  p.table_ld = table_ld;
+  p.row_to_table = row_to_table;
+  p.page_size = page_size;
+  p.out_slots = out_slots;
+  p.out_pos = out_pos;
+  p.ws = static_cast<char*>(workspace);
+  p.wait_ns = wait_ns;
+  p.skip_cta = skip_cta;
+  if (launch_select(p, grid, stream) != cudaSuccess) return TOPK_ERR_CUDA;
+  return TOPK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -108,38 +149,21 @@ int topk_select_paged(const float* scores, int64_t ld, const int32_t* lens, int 
                       int k, const int32_t* block_table, int64_t table_ld,
                       const int32_t* row_to_table, int page_size, int32_t* out_slots,
                       int32_t* out_pos, void* workspace, topk_stream_t stream) {
-  if (rows < 0) return TOPK_ERR_ROWS;
-  if (k < 1 || k > TOPK_MAX_K) return TOPK_ERR_K;
-  if (page_size < 1) return TOPK_ERR_PAGE_SIZE;
-  if (max_len < 0) return TOPK_ERR_MAX_LEN;
-  if (ld < max_len || table_ld < 1) return TOPK_ERR_LD;
-  if (!workspace) return TOPK_ERR_NULL;
-  if (rows == 0) return TOPK_OK;
-  if (!scores || !lens || !block_table || !out_slots) return TOPK_ERR_NULL;
-  if (!aligned(scores, 4) || !aligned(out_slots, 4) || (out_pos && !aligned(out_pos, 4)) ||
-      !aligned(lens, 4) || !aligned(block_table, 4) || (row_to_table && !aligned(row_to_table, 4)))
-    return TOPK_ERR_ALIGN;
-  if (!aligned(workspace, 256)) return TOPK_ERR_WORKSPACE;
-  int grid = 0;
-  const int e = device_grid(&grid);
-  if (e != TOPK_OK) return e;
-  if ((int64_t)max_len > (int64_t)grid * kChunkCap) return TOPK_ERR_MAX_LEN;
-  SelectParams p;
-  p.scores = scores;
-  p.ld = ld;
-  p.lens = lens;
-  p.rows = rows;
-  p.max_len = max_len;
-  p.k = k;
-  p.table = block_table;
-  p.table_ld = table_ld;
-  p.row_to_table = row_to_table;
-  p.page_size = page_size;
-  p.out_slots = out_slots;
-  p.out_pos = out_pos;
-  p.ws = static_cast<char*>(workspace);
-  if (launch_select(p, grid, (cudaStream_t)stream) != cudaSuccess) return TOPK_ERR_CUDA;
-  return TOPK_OK;
+  return select_common(scores, ld, lens, rows, max_len, k, block_table, table_ld, row_to_table,
+                       page_size, out_slots, out_pos, workspace, (cudaStream_t)stream, kWaitNs, -1);
+}
+
+// Test entry: topk_select_paged with a bounded-wait limit in nanoseconds (0: the
+// default 200 ms) and one CTA (skip_cta >= 0) that never arrives at its first row
+// barrier, so that the waits of the row it serves run out.
+int topk_select_paged_test(const float* scores, int64_t ld, const int32_t* lens, int rows,
+                           int max_len, int k, const int32_t* block_table, int64_t table_ld,
+                           const int32_t* row_to_table, int page_size, int32_t* out_slots,
+                           int32_t* out_pos, void* workspace, topk_stream_t stream,
+                           uint64_t wait_ns, int skip_cta) {
+  return select_common(scores, ld, lens, rows, max_len, k, block_table, table_ld, row_to_table,
+                       page_size, out_slots, out_pos, workspace, (cudaStream_t)stream,
+                       wait_ns ? wait_ns : kWaitNs, skip_cta);
 }
 
 int topk_read_status(const void* workspace, topk_stream_t stream, int* status) {

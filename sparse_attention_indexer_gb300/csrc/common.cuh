@@ -76,9 +76,13 @@ struct __align__(16) UnitDesc {
 // Per multi-CTA row. Row barriers use one flag word per rank: (barriers passed by
 // that rank) << 32 | a 32-bit payload, written with release semantics; a waiter
 // acquires every rank's flag, so a barrier also delivers each rank's payload (its
-// counts). Flags only grow and are never reset by the select kernel. The histograms
-// are cleared by the CTAs that wrote them once a later barrier shows every CTA has
-// read them; the candidate slots are overwritten by every call.
+// counts). Each rank also keeps the payloads of its last two barriers (pay2, by
+// barrier parity, stored before the flag): a rank can run at most one barrier ahead
+// of a waiter still reading its flag (it cannot pass the next barrier before that
+// waiter arrives there), and the waiter then takes the payload from pay2. Flags only
+// grow and are never reset by the select kernel. The histograms are cleared by the
+// CTAs that wrote them once a later barrier shows every CTA has read them; the
+// candidate slots and pay2 are written before they are read in every call.
 struct GroupState {
   unsigned long long flag[kMaxGrid];
   uint32_t and_key;  // ~AND of boundary keys (stored inverted: reset value 0)
@@ -88,6 +92,7 @@ struct GroupState {
   uint32_t hlev[3][1 << kLevelBits];
   uint32_t cand_key[kGroupCap];
   uint32_t cand_pos[kGroupCap];
+  uint32_t pay2[2][kMaxGrid];
 };
 static_assert(sizeof(GroupState) % 256 == 0, "group state alignment");
 
@@ -141,6 +146,8 @@ struct SelectParams {
   int32_t* out_slots;
   int32_t* out_pos;
   char* ws;
+  uint64_t wait_ns;  // limit of every bounded wait (kWaitNs unless a test shortens it)
+  int skip_cta;      // test hook: this CTA never arrives at its first row barrier (-1: none)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -198,14 +205,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, for at most kWaitNs. Returns false
+// Waits for phase `parity` of `bar` to complete, for at most wait_ns. Returns false
 // on expiry.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t wait_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitNs) return false;
+    if (global_timer_ns() - t0 > wait_ns) return false;
   }
 }
 

@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "keys.cuh"
 
 namespace topk {
 
@@ -83,53 +84,7 @@ static_assert(sizeof(int32_t) * TOPK_MAX_K + 2 * sizeof(uint32_t) * kListCap <=
                   sizeof(uint32_t) * kBins0,
               "staging lists must fit the histogram region");
 
-// ------------------------------------------------------------- keys and digits
-
-// Order-preserving 32-bit key: larger key <=> larger score. -0.0 is folded onto
-// +0.0; every NaN maps to 0, below -inf (0x007FFFFF).
-__device__ __forceinline__ uint32_t f2key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  const uint32_t a = u & 0x7FFFFFFFu;
-  if (a > 0x7F800000u) return 0u;
-  if (a == 0u) return 0x80000000u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Coarse 12-bit digit, monotone non-decreasing in the score: sign, a 5-bit exponent
-// window (|x| in [2^-15, 2^17)) and 6 mantissa bits, clamped at both ends. Equal
-// scores share a digit (-0 is folded onto +0 by adding +0); NaN is first mapped to
-// -inf, which together with every score at or below -2^17 lands in bin 0.
-__device__ __forceinline__ uint32_t coarse_digit(float x) {
-  const float xc = __fadd_rn(fmaxf(x, __int_as_float(0xFF800000)), 0.0f);
-  const float ax = fminf(fmaxf(fabsf(xc), 3.0517578125e-05f), 131071.99f);
-  const uint32_t m = (__float_as_uint(ax) >> 17) - 7168u;  // in [0, 2047]
-  const uint32_t s = (uint32_t)((int32_t)__float_as_uint(xc) >> 31);
-  return ((m ^ s) ^ 0x800u) & 0xFFFu;
-}
-
-// A float t such that x < t implies coarse_digit(x) < b (a conservative filter used
-// to skip vectors without computing digits). NaN never satisfies x < t.
-__device__ __forceinline__ float skip_below(uint32_t b) {
-  if (b == 0u) return __uint_as_float(0xFF800000u);  // -inf: nothing is skipped
-  if (b < 2048u) {
-    const uint32_t j = 2048u - b;  // (2047 - b) + 1, in [1, 2047]
-    return -__uint_as_float((j + 7168u) << 17);
-  }
-  if (b == 2048u) return 0.0f;
-  return __uint_as_float(((b - 2048u) + 7168u) << 17);
-}
-
 // ------------------------------------------------------------- block helpers
-
-__device__ __forceinline__ int warp_incl_scan(int x) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  return x;
-}
 
 // Exclusive scan over the CTA in thread order; *total gets the CTA sum.
 __device__ int block_excl_scan(int v, int* total, Smem& s) {
@@ -293,15 +248,19 @@ __device__ void fill_row(const Ctx& c, int r, int from, int to) {
 // The wait has the lanes of warp 0 acquire every rank's flag, then a CTA barrier
 // passes the ordering on; afterwards s.pay[j] holds rank j's payload, *prefix (if
 // non-null) the sum of the payloads of ranks below this one and s.bc[18] the largest
-// payload. group_wait returns false if a bounded wait expired (status set).
-__device__ uint32_t group_arrive(Unit& u, uint32_t payload) {
+// payload. group_wait returns false if a bounded wait expired (status set). Test hook:
+// CTA p.skip_cta never arrives at the first row barrier of its units, so that the
+// waits of the row it serves run out (the call then reports TOPK_STATUS_TIMEOUT).
+__device__ uint32_t group_arrive(const Ctx& c, Unit& u, uint32_t payload) {
   __syncthreads();
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0 && u.bar_seq == 0) g_select_trace[blockIdx.x * 32 + 26] = global_timer_ns();
 #endif
+  const bool skip = u.bar_seq == 0 && (int)blockIdx.x == c.p.skip_cta;
   u.bar_seq += 1;
   const uint32_t my = u.flag_base + u.bar_seq;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !skip) {
+    u.gs->pay2[my & 1u][u.rank] = payload;  // ordered before the flag by the release
     st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
   }
   return my;
@@ -319,20 +278,26 @@ __device__ bool group_wait(Ctx& c, Unit& u, uint32_t my, int* prefix) {
       if ((uint32_t)(v >> 32) < my) {
         const uint64_t t0 = global_timer_ns();
         while ((uint32_t)((v = ld_acquire_u64(&u.gs->flag[j])) >> 32) < my) {
-          if (global_timer_ns() - t0 > kWaitNs) {
+          if (global_timer_ns() - t0 > c.p.wait_ns) {
             ok = false;
             stuck = j;
             break;
           }
         }
       }
-      // A rank already past this barrier has replaced its payload: the call's result
-      // would be undefined, so it is reported (it needs a waiter to stall for longer
-      // than a rank's work between two barriers).
-      if ((uint32_t)(v >> 32) != my) overrun = true;
-      c.s.pay[j] = (uint32_t)v;
-      if (j < u.rank) acc += (int)(uint32_t)v;
-      mx = max(mx, (uint32_t)v);
+      // A rank one barrier ahead (it passed this one while this waiter was still
+      // reading other flags) has replaced the flag's payload; its pay2 entry of this
+      // barrier's parity still holds it. Two barriers ahead cannot happen (the rank
+      // would have passed a barrier this CTA has not arrived at): reported.
+      uint32_t pv = (uint32_t)v;
+      const uint32_t seen = (uint32_t)(v >> 32);
+      if (seen != my) {
+        if (seen == my + 1u) pv = __ldcg(&u.gs->pay2[my & 1u][j]);
+        else overrun = true;
+      }
+      c.s.pay[j] = pv;
+      if (j < u.rank) acc += (int)pv;
+      mx = max(mx, pv);
     }
     const bool all_ok = __all_sync(0xffffffffu, ok);
     if (__any_sync(0xffffffffu, overrun) && threadIdx.x == 0) set_status(c.h, TOPK_STATUS_ORDER);
@@ -357,7 +322,7 @@ __device__ bool group_wait(Ctx& c, Unit& u, uint32_t my, int* prefix) {
 }
 
 __device__ bool group_sync(Ctx& c, Unit& u, uint32_t payload, int* prefix) {
-  return group_wait(c, u, group_arrive(u, payload), prefix);
+  return group_wait(c, u, group_arrive(c, u, payload), prefix);
 }
 
 // Finds bin b of a 4096-bin histogram (8 bins per thread: row-wide counts g[], this
@@ -588,14 +553,22 @@ __device__ void issue_chunk(Ctx& c, Unit& u) {
   if (threadIdx.x == 0) issue_copies(c.s, src, bytes, 0, u.issued);
 }
 
+// Bounded wait for piece i. A wait that runs out sets the status and waits once more
+// (bounded); if the copy still has not landed, the CTA is marked aborting (s.bc[7],
+// with the piece and its phase in s.bc[8], s.bc[13]): it takes no further units, and
+// before it exits it waits (bounded) for that copy once more, so that no copy it
+// issued is left writing into shared memory it no longer owns.
 __device__ __forceinline__ void wait_piece(Ctx& c, int i) {
   const uint32_t par = (c.mphase >> i) & 1u;
-  if (!mbar_wait_bounded(&c.s.mbar[i], par)) {
+  if (!mbar_wait_bounded(&c.s.mbar[i], par, c.p.wait_ns)) {
     if (threadIdx.x == 0) {
       set_status(c.h, TOPK_STATUS_TIMEOUT);
       record_timeout(c.h, 2, -1, i, (int)par, 0, 0);
     }
-    mbar_wait_bounded(&c.s.mbar[i], par);
+    if (!mbar_wait_bounded(&c.s.mbar[i], par, c.p.wait_ns) && atomicExch(&c.s.bc[7], 1) == 0) {
+      c.s.bc[8] = i;
+      c.s.bc[13] = (int)par;
+    }
   }
   c.mphase ^= (1u << i);
 }
@@ -1019,6 +992,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   __syncthreads();  // histogram zeroed
   TOPK_LOG(u.r, 9);
   histogram_chunk(c, u);
+  if (s.bc[7]) return;  // a copy never landed: this CTA aborts (histogram_chunk ended in a CTA barrier)
   TOPK_MARK(g_select_trace, 2);
   TOPK_LOG(u.r, 2);
 
@@ -1283,7 +1257,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   const bool overlap = u.G > 1 && !fallback && !(compact && !slots && !stage_cand);
   int out_base = 0, cand_base = 0;
   if (overlap) {
-    const uint32_t seq = group_arrive(u, counts);
+    const uint32_t seq = group_arrive(c, u, counts);
     for (int i = threadIdx.x; i < n_emit; i += kThreads)
       slot_e[i] = lookup_slot(c, u, s.u.l.elist[i]);
     for (int i = threadIdx.x; i < n_own; i += kThreads)
@@ -1482,6 +1456,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     s.bc[26] = h2.y;  // plan_error
     s.bc[27] = h2.z;  // n_implicit
     s.bc[28] = h2.w;  // dyn_period
+    s.bc[7] = 0;      // no aborting copy
     for (int i = 0; i < kPieces; ++i) mbar_init(&s.mbar[i], 1);
     fence_mbar_init();
     // Start the first static unit's copies right away when the plan is valid.
@@ -1525,6 +1500,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   Ctx c{p, h, s, 0u};
   for (int w = 0; w < waves; ++w) {
     UnitDesc d;
+    __syncthreads();
+    if (s.bc[7]) break;
     if (w == 0) {
       d = s.ud;
     } else {
@@ -1545,6 +1522,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   bool implicit = idx >= 0;
   const bool tickets = n_single > n_implicit;
   while (true) {
+    __syncthreads();
+    if (s.bc[7]) break;
     if (!implicit && !tickets) break;
     if (!implicit) {
       __syncthreads();
@@ -1569,6 +1548,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     d.pad = 0;
     process_unit(c, d, false);
   }
+  __syncthreads();
+  if (s.bc[7] && threadIdx.x == 0)  // the copy that never landed: one more bounded wait
+    mbar_wait_bounded(&s.mbar[s.bc[8]], (uint32_t)s.bc[13], p.wait_ns);
   TOPK_MARK(g_select_trace, 9);
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0) g_select_log_n[blockIdx.x] = trace_log_n();

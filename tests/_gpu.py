@@ -18,7 +18,8 @@ def to_dev(b, ld=None):
     return scores, lens, table, r2t
 
 
-def run_gpu(b, k=None, chunk=0, with_pos=True, guard=64, plan=None, dev_inputs=None):
+def run_gpu(b, k=None, chunk=0, with_pos=True, guard=64, plan=None, dev_inputs=None,
+            wait_ns=None, skip_cta=-1):
     """Returns (slots, pos or None, status) as numpy arrays. Output buffers carry guard
     canaries on both sides which must stay untouched."""
     from sparse_attention_indexer_gb300 import PagedTopK
@@ -33,7 +34,13 @@ def run_gpu(b, k=None, chunk=0, with_pos=True, guard=64, plan=None, dev_inputs=N
     pbuf = torch.full((n + 2 * guard,), -777, dtype=torch.int32, device=scores.device)
     out_s = sbuf[guard:guard + n].view(rows, k)
     out_p = pbuf[guard:guard + n].view(rows, k) if with_pos else None
-    core.select(scores, lens, k, table, b.page_size, r2t, out_slots=out_s, out_pos=out_p)
+    if wait_ns is None:
+        core.select(scores, lens, k, table, b.page_size, r2t, out_slots=out_s, out_pos=out_p)
+    else:
+        from sparse_attention_indexer_gb300 import binding as B
+        B.topk_select_paged_test(scores, scores.stride(0), lens, rows, b.max_len, k, table,
+                                 table.stride(0), r2t, b.page_size, out_s, out_p, core.workspace,
+                                 wait_ns, skip_cta)
     status = core.status()
     if status & 16:
         diag = core.workspace[128:160].cpu().numpy().view(np.int32)

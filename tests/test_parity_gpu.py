@@ -216,10 +216,16 @@ def test_device_plan_matches_host_reference():
     # lengths alone (the plan reads nothing else): more than grid * 48128 values over
     # <= 64 rows start the search at the chunk cap, where nothing fits one wave
     import types
+    rng = np.random.default_rng(44)
+    spread = lambda n: np.exp(rng.uniform(np.log(16), np.log(30000), n)).astype(int).tolist()  # noqa: E731
+    # many-bucket batches ranked in one pass over 2 and 3 rounds of 256 rows; and one
+    # whose 530 split rows exceed the group states (plan error: every row ranked single)
+    err_rows = [49_000 + 21 * i for i in range(530)] + [int(1.5 * 2 ** (4 + i % 10)) for i in range(70)]
     big = [types.SimpleNamespace(lens=np.array(l, np.int32), rows=len(l), max_len=max(l))
            for l in ([1_000_000] * 8, [300_000] * 32, [1_900_000] * 4, [7_000_000, 10],
                      [48_128 * 21] * 7, [48_127] * 32, [200_000] * 50, [48_127] * 64,
-                     [3000 + 977 * i for i in range(63)])]
+                     [3000 + 977 * i for i in range(63)], spread(500), spread(700),
+                     err_rows)]
     for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, more,
               W.tiny_rows()[0], W.tiny_rows()[15], W.prefill(), *big):
         lens = torch.from_numpy(b.lens).cuda()
@@ -230,6 +236,8 @@ def test_device_plan_matches_host_reference():
         B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img_host)
         hd, rd, sd, (fd, ud), info = parse_plan(img_dev, b.rows)
         hh, rh, sh, (fh, uh), _ = parse_plan(img_host, b.rows)
+        if b.rows == len(err_rows) and b.max_len > 48_128:
+            assert hh["plan_error"] == 1
         assert hd == hh
         assert np.array_equal(rd, rh)
         assert np.array_equal(sd[:hh["n_single"]], sh[:hh["n_single"]])

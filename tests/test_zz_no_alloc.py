@@ -70,8 +70,44 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         rp, rs = _by_position(ref_p, ref_s)
         assert np.array_equal(gp, rp), f"call {i}: positions differ from the workspace path"
         assert np.array_equal(gs, rs), f"call {i}: slots differ from the workspace path"
-    s, p, _ = calls[0].result()
-    compare_with_oracle(a, a.k, s, p)
+        compare_with_oracle(call.b, call.k, s, p)
+
+
+def test_noalloc_status_reaches_the_caller_and_the_next_call_clears_it():
+    """Device status bits of a call arrive in the caller's status word; the next call
+    starts from a clean status. rows == 0 and status == NULL are accepted."""
+    rng = np.random.default_rng(2)
+    L = 6000
+    s = rng.standard_normal((3, L)).astype(np.float32)
+    tab = np.stack([rng.permutation(L // 64 + 1).astype(np.int32) for _ in range(3)])
+    s[1, 64:128] = 50.0
+    tab[1, 1] = -3  # the selected positions of row 1 map to a negative page
+    bad = W.Batch("bad_entry", s, np.full(3, L, np.int32), L, 16, tab, None, 64)
+    call = _Call(bad, 16)
+    assert call.run() == 0
+    sl, p, st = call.result()
+    assert st == B.STATUS_TABLE_ENTRY, B.status_str(st)
+    compare_with_oracle(bad, 16, sl, p)  # the oracle writes -1 for those entries too
+    clean = _Call(W.pr1(), 2048)
+    assert clean.run() == 0
+    sl, p, st = clean.result()
+    assert st == 0
+    compare_with_oracle(clean.b, 2048, sl, p)
+    # rows == 0: nothing to select; the status word is cleared
+    zero = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    assert B.topk_select_paged_noalloc(None, 16, None, 0, 16, 1, None, 1, None, 64, None, None,
+                                       zero) == 0
+    torch.cuda.synchronize()
+    assert int(zero.item()) == 0
+    # status == NULL: the call still runs
+    b = clean.b
+    clean.slots.fill_(-5)
+    clean.pos.fill_(-5)
+    assert B.topk_select_paged_noalloc(clean.scores, b.ld, clean.lens, b.rows, b.max_len, 2048,
+                                       clean.table, b.block_table.shape[1], clean.r2t,
+                                       b.page_size, clean.slots, clean.pos, None) == 0
+    sl, p, _ = clean.result()
+    compare_with_oracle(b, 2048, sl, p)
 
 
 def test_noalloc_rejects_rows_above_limit():
