@@ -15,6 +15,8 @@ int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_fo
 cudaError_t launch_select(const SelectParams& p, int grid, cudaStream_t stream);
 size_t select_smem_bytes();
 const void* select_kernel_ptr();
+int short_max_len();
+cudaError_t launch_short(const SelectParams& p, cudaStream_t stream);
 }  // namespace topk
 
 using namespace topk;
@@ -108,6 +110,9 @@ int select_common(const float* scores, int64_t ld, const int32_t* lens, int rows
   p.ws = static_cast<char*>(workspace);
   p.wait_ns = wait_ns;
   p.skip_cta = skip_cta;
+  // Batches of short rows take the register-resident path (one warp per row); the
+  // plan's header is still checked there.
+  if (max_len <= short_max_len()) return launch_short(p, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
   if (launch_select(p, grid, stream) != cudaSuccess) return TOPK_ERR_CUDA;
   return TOPK_OK;
 }

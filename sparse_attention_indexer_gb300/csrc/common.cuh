@@ -31,6 +31,7 @@ constexpr int kGroupCap = 8192;            // multi-CTA compact candidate list (
 constexpr int kListBins = 256;             // digit width 8 for list refinement
 constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
 constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // bounded waits: 200 ms
+constexpr int kShortMaxLen = 256;          // batches with max_len <= this: register path
 
 // ---------------------------------------------------------------- workspace
 // All offsets are multiples of 256 bytes.

@@ -778,8 +778,32 @@ extern "C" int topk_trace_plan(uint64_t* host, int n) {
 }
 #endif
 
+// Plan of a batch of short rows (max_len <= kShortMaxLen, the register path: one warp
+// per row, no work list): the header alone, which the select kernel checks.
+__global__ void short_plan_kernel(int rows, int max_len, int grid, char* ws) {
+  if (threadIdx.x != 0) return;
+  Header* h = reinterpret_cast<Header*>(ws);
+  h->magic = kMagic;
+  h->rows = rows;
+  h->max_len = max_len;
+  h->grid = grid;
+  h->chunk = 0;
+  h->waves = 0;
+  h->n_single = rows;
+  h->n_multi = 0;
+  h->status = 0;
+  h->plan_error = 0;
+  h->n_implicit = 0;
+  h->dyn_period = 0;
+  for (int i = 0; i < 8; ++i) h->diag[i] = 0;
+}
+
 cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, int chunk_force,
                         void* ws, cudaStream_t stream) {
+  if (max_len <= kShortMaxLen && chunk_force == 0) {
+    short_plan_kernel<<<1, 32, 0, stream>>>(rows, max_len, grid, static_cast<char*>(ws));
+    return cudaGetLastError();
+  }
   const Layout lay = make_layout(rows);
   const size_t n16 = offsetof(GroupState, cand_key) / 16 * (size_t)lay.ngroups;
   const size_t per_block = (size_t)kPlanThreads * kZeroPerThread;
@@ -797,6 +821,15 @@ cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, in
 int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_force, char* ws) {
   const Layout lay = make_layout(rows);
   Header* h = reinterpret_cast<Header*>(ws + lay.header);
+  if (max_len <= kShortMaxLen && chunk_force == 0) {  // the register path: header only
+    *h = Header{};
+    h->magic = kMagic;
+    h->rows = rows;
+    h->max_len = max_len;
+    h->grid = grid;
+    h->n_single = rows;
+    return 0;
+  }
   RowInfo* ri = reinterpret_cast<RowInfo*>(ws + lay.rowinfo);
   int2* singles = reinterpret_cast<int2*>(ws + lay.singles);
   int32_t* first_single = reinterpret_cast<int32_t*>(ws + lay.first_single);

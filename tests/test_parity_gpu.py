@@ -236,6 +236,9 @@ def test_device_plan_matches_host_reference():
         B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img_host)
         hd, rd, sd, (fd, ud), info = parse_plan(img_dev, b.rows)
         hh, rh, sh, (fh, uh), _ = parse_plan(img_host, b.rows)
+        if b.max_len <= 256:  # register path: the plan is its header alone
+            assert hd == hh
+            continue
         if b.rows == len(err_rows) and b.max_len > 48_128:
             assert hh["plan_error"] == 1
         assert hd == hh

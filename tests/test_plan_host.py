@@ -18,6 +18,7 @@ S = pytest.importorskip("sparse_attention_indexer_gb300")
 B = S.binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SHORT_MAX_LEN = 256  # batches whose rows are at most this long take the register path
 
 
 def _lib_or_skip():
@@ -75,6 +76,12 @@ def check_plan(lens, max_len, grid, chunk=0):
     counts one claim per remaining single row plus one failing claim per CTA."""
     _lib_or_skip()
     hdr, ri, singles, (first, units), info = host_plan(lens, max_len, grid, chunk)
+    if max_len <= SHORT_MAX_LEN and chunk == 0:
+        # register path (one warp per row): the plan is its header alone
+        assert hdr["magic"] == 0x54504B32 and hdr["rows"] == len(lens)
+        assert hdr["max_len"] == max_len and hdr["status"] == 0 and hdr["plan_error"] == 0
+        assert hdr["waves"] == 0 and hdr["n_multi"] == 0 and hdr["n_single"] == len(lens)
+        return hdr, None
     rows = len(lens)
     assert hdr["magic"] == 0x54504B32 and hdr["rows"] == rows and hdr["grid"] == grid
     assert hdr["plan_error"] == 0
@@ -168,9 +175,11 @@ def test_plan_forced_chunks(chunk):
 
 
 def test_plan_degenerate_lengths():
-    check_plan(np.array([0, 0, 0], np.int32), 100, 152)
-    check_plan(np.array([-5, 101, 50], np.int32), 100, 152)  # invalid lengths become single rows
-    check_plan(np.array([], np.int32).reshape(0), 100, 152)
+    check_plan(np.array([0, 0, 0], np.int32), 300, 152)
+    check_plan(np.array([-5, 301, 50], np.int32), 300, 152)  # invalid lengths become single rows
+    check_plan(np.array([], np.int32).reshape(0), 300, 152)
+    check_plan(np.array([-5, 101, 50], np.int32), 100, 152)  # register path: header only
+    check_plan(np.array([0, 0, 0], np.int32), 100, 152, chunk=16)  # forced: full plan
     rng = np.random.default_rng(3)
     lens = rng.integers(0, 300_000, size=400).astype(np.int32)
     check_plan(lens, 300_000, 152)
