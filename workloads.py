@@ -453,3 +453,114 @@ def hisparse(seed: int = SEED_BASE + 7, reqs: int = 8, k: int = 2048, page_size:
         steps.append(sel)
     return ResolverBatch("hisparse", tab, page_size, lens.astype(np.int32), hot_rows, kv_rows,
                          row_bytes, host_kv, host_base, kv_init, steps)
+
+
+# ---------------------------------------------------------------- indexer MQA logits
+@dataclasses.dataclass
+class LogitsBatch:
+    """Inputs of one call of the indexer score producer (MQA logits over the paged FP8
+    key cache) and of the top-k selection that consumes its score rows.
+
+    Query rows come in groups of `group_rows` consecutive rows (the tokens of one
+    request: a decode token and its draft tokens, or a prefill chunk); every row of
+    group g reads the keys of block-table row group_table[g] (g itself when
+    group_table is None), each up to its own valid length."""
+
+    name: str
+    q: np.ndarray             # uint8 [rows, H, D]: e4m3 codes of the per-head queries
+    w: np.ndarray             # float32 [rows, H]: head-gate weights
+    cache: np.ndarray         # uint8 [num_slots, D]: e4m3 codes of the keys
+    cache_scale: np.ndarray   # float32 [num_slots]: per-key scales
+    lens: np.ndarray          # int32 [rows]: keys each query row scores
+    max_len: int
+    group_rows: int
+    group_table: Optional[np.ndarray]  # int32 [n_groups] or None
+    block_table: np.ndarray   # int32 [n_tables, table_ld]
+    page_size: int
+    k: int = 2048
+
+    @property
+    def rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def dim(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def num_slots(self) -> int:
+        return int(self.cache.shape[0])
+
+    def row_to_table(self) -> np.ndarray:
+        """Block-table row of every query row (int32 [rows])."""
+        g = np.arange(self.rows) // self.group_rows
+        t = g if self.group_table is None else self.group_table[g]
+        return np.asarray(t, np.int32)
+
+    def flops(self) -> int:
+        """Multiply-adds of the query-key products, counted as 2 FLOPs each: every
+        head of every row against each of the row's keys."""
+        return 2 * int(self.lens.astype(np.int64).clip(0).sum()) * self.heads * self.dim
+
+
+def e4m3_codes(rng: np.random.Generator, shape, exp_mean: float, exp_sd: float) -> np.ndarray:
+    """Random e4m3 bit patterns: a fair sign bit, an exponent field drawn as
+    round(N(exp_mean, exp_sd)) clipped to [0, 15], a uniform 3-bit mantissa; the
+    NaN pattern (exponent 15, mantissa 7) becomes mantissa 6 (the largest finite)."""
+    sign = rng.integers(0, 2, size=shape).astype(np.uint8) << 7
+    e = np.clip(np.rint(rng.normal(exp_mean, exp_sd, size=shape)), 0, 15).astype(np.uint8)
+    m = rng.integers(0, 8, size=shape).astype(np.uint8)
+    m = np.where((e == 15) & (m == 7), np.uint8(6), m)
+    return (sign | (e << 3) | m).astype(np.uint8)
+
+
+def logits_batch(name: str, seed: int, lens, group_rows: int, heads: int = 64, dim: int = 128,
+                 page_size: int = 64, n_tables: Optional[int] = None, spare_pages: int = 0,
+                 k: int = 2048) -> LogitsBatch:
+    """Query rows with the given valid lengths, in groups of `group_rows`. Each group
+    gets its own block-table row (a shuffled set of physical pages from one pool;
+    group_table is a permutation when n_tables > groups, else None); the cache holds
+    the pool's pages plus `spare_pages` unused ones.
+
+    Codes stand in for per-token-scaled FP8 tensors, whose largest element sits near
+    448: key exponent fields N(13, 1.5), query fields N(12, 1.5); key scales
+    exp(N(-6, 0.3)) (about 1/400, an amax near 1); head gates N(0, 1) / 64."""
+    rng = _rng(seed)
+    lens = np.asarray(lens, np.int32)
+    rows = len(lens)
+    n_groups = -(-rows // group_rows)
+    glen = [int(lens[g * group_rows:(g + 1) * group_rows].clip(0).max()) for g in range(n_groups)]
+    max_len = int(lens.max()) if rows else 0
+    table_ld = max(1, -(-max_len // page_size))
+    need = [-(-L // page_size) for L in glen]
+    pool = _shuffled_pages(rng, sum(need) + spare_pages)
+    nt = n_groups if n_tables is None else max(n_tables, n_groups)
+    tab = np.full((nt, table_ld), -1, np.int32)
+    gt = None
+    if nt > n_groups:
+        gt = rng.permutation(nt)[:n_groups].astype(np.int32)
+    at = 0
+    for g, m in enumerate(need):
+        tab[g if gt is None else gt[g], :m] = pool[at:at + m]
+        at += m
+    num_slots = (sum(need) + spare_pages) * page_size
+    cache = e4m3_codes(rng, (num_slots, dim), 13.0, 1.5)
+    scale = np.exp(rng.normal(-6.0, 0.3, num_slots)).astype(np.float32)
+    q = e4m3_codes(rng, (rows, heads, dim), 12.0, 1.5)
+    w = (rng.standard_normal((rows, heads)) / 64.0).astype(np.float32)
+    return LogitsBatch(name, q, w, cache, scale, lens, max_len, group_rows, gt, tab, page_size, k)
+
+
+def logits_verify_80k(seed: int = SEED_BASE + 8) -> LogitsBatch:
+    """bs=1 MTP target verify at 80K context: 7 query rows (1 + 6 draft tokens) of one
+    request, causal lengths 80000..80006, 64 heads of 128 channels, pages of 64."""
+    return logits_batch("logits_verify_80k", seed, np.arange(80000, 80007), 7)
+
+
+def logits_verify_1m(seed: int = SEED_BASE + 9) -> LogitsBatch:
+    """The same at 1M context: lengths 1,000,000..1,000,006."""
+    return logits_batch("logits_verify_1m", seed, np.arange(1000000, 1000007), 7)
