@@ -33,7 +33,7 @@ EXPORTS = (
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
     "topk_select_paged_noalloc", "indexer_k_prologue", "hisparse_resolve",
-    "topk_select_paged_test",
+    "topk_select_paged_test", "indexer_mqa_logits",
 )
 
 
@@ -69,6 +69,9 @@ _SIGS = {
     "indexer_k_prologue": (_c.c_int, [_VP, _c.c_int64, _c.c_int, _c.c_int, _VP, _VP, _c.c_float,
                                       _VP, _VP, _c.c_int, _c.c_int, _VP, _VP, _c.c_int,
                                       _c.c_int64, _c.c_int, _VP, _VP, _c.c_int64, _VP, _VP]),
+    "indexer_mqa_logits": (_c.c_int, [_VP, _VP, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_int,
+                                      _c.c_int, _VP, _VP, _c.c_int, _c.c_int, _c.c_int, _VP, _VP,
+                                      _c.c_int64, _VP, _c.c_int64, _VP, _VP]),
     "hisparse_resolve": (_c.c_int, [_VP, _c.c_int, _c.c_int, _VP, _c.c_int64, _c.c_int, _VP,
                                     _c.c_int64, _VP, _VP, _VP, _c.c_int, _c.c_int, _VP, _VP,
                                     _c.c_int64, _VP, _c.c_int64, _c.c_int, _VP, _VP, _VP, _VP]),
@@ -242,6 +245,44 @@ def indexer_k_prologue(k, ln_w, ln_b, eps: float, positions, cos_sin, rope_dim: 
         _ptr(cache), _ptr(cache_scale), int(cache.shape[0]), _ptr(status), _stream(stream))
     if code < 0:
         raise PrologueError(code)
+    return code
+
+
+# include/indexer_logits.h
+LOGITS_ERR_NULL = -1
+LOGITS_ERR_SHAPE = -2
+LOGITS_ERR_ALIGN = -3
+LOGITS_ERR_CUDA = -4
+LOGITS_STATUS_LEN = 1
+LOGITS_STATUS_TABLE_WIDTH = 2
+LOGITS_STATUS_TABLE_ENTRY = 4
+LOGITS_STATUS_SLOT = 8
+LOGITS_STATUS_TABLE_ROW = 16
+LOGITS_STATUS_TIMEOUT = 32
+
+
+class LogitsError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__(f"indexer_mqa_logits: {code}")
+        self.code = code
+
+
+def indexer_mqa_logits(q, w, lens, max_len: int, group_rows: int, group_table, block_table,
+                       page_size: int, cache, cache_scale, scores, status=None,
+                       stream=None) -> int:
+    """indexer_mqa_logits of include/indexer_logits.h on CUDA tensors: q uint8 [rows,
+    heads, dim], w float32 [rows, heads], lens int32 [rows], group_table int32 [groups]
+    or None, block_table int32 [n_tables, table_ld], cache uint8 [num_slots, dim],
+    cache_scale float32 [num_slots], scores float32 [rows, ld], status int32 [1] or
+    None. Argument marshalling only."""
+    rows, heads, dim = (int(x) for x in q.shape)
+    code = lib().indexer_mqa_logits(
+        _ptr(q), _ptr(w), rows, heads, dim, _ptr(lens), int(max_len), int(group_rows),
+        _ptr(group_table), _ptr(block_table), int(block_table.shape[0]),
+        int(block_table.stride(0)), int(page_size), _ptr(cache), _ptr(cache_scale),
+        int(cache.shape[0]), _ptr(scores), int(scores.stride(0)), _ptr(status), _stream(stream))
+    if code < 0:
+        raise LogitsError(code)
     return code
 
 

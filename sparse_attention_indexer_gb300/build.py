@@ -1,8 +1,8 @@
 """Builds the CUDA library libtopk_paged.so in-tree for sm_103a with nvcc.
 
-Seven translation units are compiled in parallel and linked into one shared library
-that exports the C ABI of include/topk_paged.h, include/indexer_prologue.h and
-include/hisparse_resolver.h (no torch types cross it).
+Eight translation units are compiled in parallel and linked into one shared library
+that exports the C ABI of include/topk_paged.h, include/indexer_prologue.h,
+include/indexer_logits.h and include/hisparse_resolver.h (no torch types cross it).
 """
 from __future__ import annotations
 
@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
-SOURCES = ["select.cu", "short.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu", "resolver.cu"]
+SOURCES = ["select.cu", "short.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu", "resolver.cu",
+           "logits.cu"]
 HEADERS = ["common.cuh", "keys.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -51,6 +52,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     os.makedirs(bdir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", h)
                                                         for h in ("topk_paged.h", "indexer_prologue.h",
+                                                                  "indexer_logits.h",
                                                                   "hisparse_resolver.h")]
     objs = []
     jobs = []

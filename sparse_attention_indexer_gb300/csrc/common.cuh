@@ -78,9 +78,10 @@ struct __align__(16) UnitDesc {
 // that rank) << 32 | a 32-bit payload, written with release semantics; a waiter
 // acquires every rank's flag, so a barrier also delivers each rank's payload (its
 // counts). Each rank also keeps the payloads of its last two barriers (pay2, by
-// barrier parity, stored before the flag): a rank can run at most one barrier ahead
-// of a waiter still reading its flag (it cannot pass the next barrier before that
-// waiter arrives there), and the waiter then takes the payload from pay2. Flags only
+// barrier parity, stored right after the flag, so that the next flag's release
+// orders it): a rank can run at most one barrier ahead of a waiter still reading its
+// flag (it cannot pass the next barrier before that waiter arrives there), and the
+// waiter, seeing that next flag, then takes the payload from pay2. Flags only
 // grow and are never reset by the select kernel. The histograms are cleared by the
 // CTAs that wrote them once a later barrier shows every CTA has read them; the
 // candidate slots and pay2 are written before they are read in every call.

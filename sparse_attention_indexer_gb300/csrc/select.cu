@@ -260,8 +260,11 @@ __device__ uint32_t group_arrive(const Ctx& c, Unit& u, uint32_t payload) {
   u.bar_seq += 1;
   const uint32_t my = u.flag_base + u.bar_seq;
   if (threadIdx.x == 0 && !skip) {
-    u.gs->pay2[my & 1u][u.rank] = payload;  // ordered before the flag by the release
     st_release_u64(&u.gs->flag[u.rank], ((unsigned long long)my << 32) | payload);
+    // The payload history is read only by a waiter that finds this flag one barrier
+    // ahead; the next release orders this store before that flag. Storing it after
+    // the release keeps it off this barrier's critical path.
+    __stcg(&u.gs->pay2[my & 1u][u.rank], payload);
   }
   return my;
 }
@@ -1498,20 +1501,23 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
 
   const bool pre_issued = s.bc[19] != 0;
   Ctx c{p, h, s, 0u};
+  bool ran = false;  // a unit ran: s.bc[7] (aborting) is read after a CTA barrier
   for (int w = 0; w < waves; ++w) {
     UnitDesc d;
-    __syncthreads();
-    if (s.bc[7]) break;
     if (w == 0) {
       d = s.ud;
     } else {
       __syncthreads();
+      if (ran && s.bc[7]) break;
       if (threadIdx.x == 0) s.ud = units[(int64_t)w * kMaxGrid + blockIdx.x];
       __syncthreads();
       d = s.ud;
     }
     TOPK_LOG(d.row, 15);
-    if (d.row >= 0) process_unit(c, d, w == 0 && pre_issued);
+    if (d.row >= 0) {
+      process_unit(c, d, w == 0 && pre_issued);
+      ran = true;
+    }
   }
 
   const int2* singles = reinterpret_cast<const int2*>(p.ws + lay.singles);
@@ -1522,9 +1528,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   bool implicit = idx >= 0;
   const bool tickets = n_single > n_implicit;
   while (true) {
-    __syncthreads();
-    if (s.bc[7]) break;
     if (!implicit && !tickets) break;
+    if (ran) {
+      __syncthreads();
+      if (s.bc[7]) break;
+    }
     if (!implicit) {
       __syncthreads();
       if (threadIdx.x == 0) {
@@ -1547,10 +1555,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
     d.group = -1;
     d.pad = 0;
     process_unit(c, d, false);
+    ran = true;
   }
-  __syncthreads();
-  if (s.bc[7] && threadIdx.x == 0)  // the copy that never landed: one more bounded wait
-    mbar_wait_bounded(&s.mbar[s.bc[8]], (uint32_t)s.bc[13], p.wait_ns);
+  if (ran) {
+    __syncthreads();
+    if (s.bc[7] && threadIdx.x == 0)  // the copy that never landed: one more bounded wait
+      mbar_wait_bounded(&s.mbar[s.bc[8]], (uint32_t)s.bc[13], p.wait_ns);
+  }
   TOPK_MARK(g_select_trace, 9);
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0) g_select_log_n[blockIdx.x] = trace_log_n();

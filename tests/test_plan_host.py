@@ -29,7 +29,7 @@ def _lib_or_skip():
 
 def header_exports():
     names = set()
-    for h in ("topk_paged.h", "indexer_prologue.h", "hisparse_resolver.h"):
+    for h in ("topk_paged.h", "indexer_prologue.h", "indexer_logits.h", "hisparse_resolver.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         names |= set(re.findall(r"\b((?:topk|indexer|hisparse)_[a-z_]+)\s*\(", src))
