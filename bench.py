@@ -52,6 +52,30 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def _logits_traffic():
+    """DRAM bytes per indexer_mqa_logits launch on the 1M verify shape from the
+    committed ncu summary, if it was taken on the current logits kernel source."""
+    path = os.path.join(ROOT, "profiles", "logits_traffic.txt")
+    src = os.path.join(ROOT, "sparse_attention_indexer_gb300", "csrc", "logits.cu")
+    try:
+        want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        vals = dict(l.split(" = ", 1) for l in open(path).read().splitlines()
+                    if " = " in l and not l.startswith("#"))
+        if vals.get("logits_cu_sha256_16") != want:
+            return None
+        return int(vals["dram_bytes_per_launch_1m"])
+    except Exception:
+        return None
+
+
 def _traffic_for_current_kernel():
     """DRAM bytes per select launch from the committed ncu summary, if it was taken on
     the current select kernel source (else None)."""
@@ -180,6 +204,116 @@ class _Batch:
         with torch.cuda.graph(self.g_select, stream=s):
             self.select()
         torch.cuda.synchronize()
+
+
+class _Logits:
+    """Device copies of one indexer score-producer batch, the score rows it writes, and
+    two CUDA graphs: the producer alone, and producer + topk_plan + topk_select_paged."""
+
+    def __init__(self, b, dev):
+        import torch
+        from sparse_attention_indexer_gb300 import PagedTopK
+        self.b = b
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.q, self.w, self.lens = t(b.q), t(b.w), t(b.lens)
+        self.gt = None if b.group_table is None else t(b.group_table)
+        self.table, self.cache, self.scale = t(b.block_table), t(b.cache), t(b.cache_scale)
+        self.r2t = t(b.row_to_table())
+        self.scores = torch.full((b.rows, W.round_up(max(b.max_len, 1), 4)), 0.0,
+                                 dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.core = PagedTopK(b.rows, b.max_len, dev)
+        self.out = torch.empty((b.rows, b.k), dtype=torch.int32, device=dev)
+
+    def produce(self):
+        from sparse_attention_indexer_gb300 import binding as Bd
+        Bd.indexer_mqa_logits(self.q, self.w, self.lens, self.b.max_len, self.b.group_rows,
+                              self.gt, self.table, self.b.page_size, self.cache, self.scale,
+                              self.scores, self.status)
+
+    def step(self):
+        self.produce()
+        self.core.plan(self.lens)
+        self.core.select(self.scores, self.lens, self.b.k, self.table, self.b.page_size,
+                         self.r2t, out_slots=self.out)
+
+    def capture(self):
+        import torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.g_prod = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_prod, stream=s):
+            self.produce()
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step, stream=s):
+            self.step()
+        torch.cuda.synchronize()
+
+
+def _logits_cpu_baseline(b, positions=20000):
+    """The fp64 oracle on one row's first `positions` keys: TFLOP/s on this host."""
+    from oracle import logits as LG
+    LG.scores_at(b, 0, np.arange(1000))  # warm
+    t0 = time.perf_counter()
+    LG.scores_at(b, 0, np.arange(positions))
+    dt = time.perf_counter() - t0
+    fl = 2 * positions * b.heads * b.dim
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+            "kind": "oracle", "sample": f"row 0 of {b.name}, positions 0..{positions - 1} "
+                                        f"({fl / 1e9:.2f} GFLOP) in {dt:.2f} s"}
+
+
+def _time_logits(dev, flush, n_calls):
+    """§8(f) NEXT-2: indexer_mqa_logits alone and feeding plan + select, as CUDA graphs,
+    L2 flushed before each call; device statuses checked first."""
+    from sparse_attention_indexer_gb300 import binding as Bd
+    import torch
+    bf16, bf16_kind = _bf16_peak()
+    peak = 2.0 * bf16
+    res = {}
+    for name, b in (("verify_80k", W.logits_verify_80k()), ("verify_1m", W.logits_verify_1m())):
+        x = _Logits(b, dev)
+        x.step()
+        torch.cuda.synchronize()
+        if int(x.status.item()) != 0 or x.core.status() != 0:
+            raise RuntimeError(f"logits {name}: status {int(x.status.item())} / "
+                               f"{Bd.status_str(x.core.status())}")
+        x.capture()
+        _time(x.g_prod.replay, 3, flush)
+        prod = _time(x.g_prod.replay, n_calls, flush, f"logits_{name}")
+        step = _time(x.g_step.replay, n_calls, flush, f"logits_topk_{name}")
+        us = float(np.mean(prod)) * 1e3
+        tf = b.flops() / (us * 1e-6) / 1e12
+        res[name] = {
+            "rows": b.rows, "heads": b.heads, "dim": b.dim, "keys_per_row": [int(b.lens.min()),
+                                                                            int(b.lens.max())],
+            "producer_us": round(us, 2), "producer_p10_p90": [
+                round(float(np.percentile(prod, 10)) * 1e3, 2),
+                round(float(np.percentile(prod, 90)) * 1e3, 2)],
+            "producer_plan_select_us": round(float(np.mean(step)) * 1e3, 2),
+            "tflops": round(tf, 1), "frac": round(tf / peak, 4),
+        }
+        if name == "verify_1m":
+            res["roofline"] = {
+                "bound": "tensor", "achieved": round(tf, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": _logits_traffic(),
+                "kernel": "logits_kernel (indexer_mqa_logits), verify_1m shape",
+                "flops_per_launch": b.flops(),
+                "peak_source": f"{bf16_kind} bf16 burst (MEASURED_PEAKS.json bf16_tflops) x 2, "
+                               "the nominal e4m3 / bf16 dense ratio",
+            }
+            res["cpu_baseline"] = _logits_cpu_baseline(b)
+        del x
+    res["workload"] = ("indexer score producer: 7 query rows (bs=1 MTP verify) x 64 e4m3 heads "
+                       "x 128 channels, per-head fp32 gates, e4m3 keys with per-key scales in a "
+                       "paged cache (pages of 64, shuffled); score = sk * sum_h g_h * "
+                       "max(0, q_h . k); the step feeds the rows to topk_plan + "
+                       "topk_select_paged (k=2048)")
+    return res
 
 
 class _Flush:
@@ -565,6 +699,9 @@ def run_ours(args):
     rv_copy = int(rv_counts[:, 2].sum()) * rb.row_bytes
     del rv
 
+    # §8(f) NEXT-2: the score producer on the tensor cores, alone and feeding the selection
+    logits_res = _time_logits(dev, flush, max(10, min(nsec, 50)))
+
     # end to end through the public API on pinned host buffers
     e2e = None
     try:
@@ -671,6 +808,7 @@ def run_ours(args):
             "host_read_gbs": round(rv_copy / (rv_ms / 1e3) / 1e9, 2),
             "bound": "latency (one CTA per request: classify, LRU sort, host round trip)",
         },
+        "logits": logits_res,
         "prefill": {
             "workload": "ragged prefill: one request, 8192 cached + 4096 new tokens; row i "
                         "scores the causal prefix 8192 + i + 1 (4096 rows, 8193..12288 fp32 "

@@ -42,7 +42,8 @@ enum {
   LOGITS_ERR_SHAPE = -2,  /* rows < 0, heads != 64, dim != 128, group_rows outside
                              [1, 8], max_len < 0, n_tables < 1, table_ld < 1,
                              page_size not a positive multiple of 64, num_slots outside
-                             [1, 2^31), ld < max_len */
+                             [1, 2^31), ld < max_len, or ceil(rows / G) *
+                             ceil(max_len / 128) >= 2^31 */
   LOGITS_ERR_ALIGN = -3,  /* q, w, cache or cache_scale not 16-byte aligned, or
                              another array not 4-byte aligned */
   LOGITS_ERR_CUDA = -4    /* a launch, the device query or the tensor-map encoding
