@@ -17,6 +17,8 @@ size_t select_smem_bytes();
 const void* select_kernel_ptr();
 int short_max_len();
 cudaError_t launch_short(const SelectParams& p, cudaStream_t stream);
+int medium_max_len();
+cudaError_t launch_medium(const SelectParams& p, int sms, cudaStream_t stream);
 }  // namespace topk
 
 using namespace topk;
@@ -110,9 +112,12 @@ int select_common(const float* scores, int64_t ld, const int32_t* lens, int rows
   p.ws = static_cast<char*>(workspace);
   p.wait_ns = wait_ns;
   p.skip_cta = skip_cta;
-  // Batches of short rows take the register-resident path (one warp per row); the
-  // plan's header is still checked there.
+  // Batches of short rows take the register-resident path (one warp per row), batches
+  // of medium rows the medium path (one CTA per row, several per SM); the plan's header
+  // is still checked there. `grid` is one CTA per SM.
   if (max_len <= short_max_len()) return launch_short(p, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+  if (max_len <= medium_max_len())
+    return launch_medium(p, grid, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
   if (launch_select(p, grid, stream) != cudaSuccess) return TOPK_ERR_CUDA;
   return TOPK_OK;
 }

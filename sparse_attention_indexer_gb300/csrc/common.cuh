@@ -32,6 +32,7 @@ constexpr int kListBins = 256;             // digit width 8 for list refinement
 constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
 constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // bounded waits: 200 ms
 constexpr int kShortMaxLen = 256;          // batches with max_len <= this: register path
+constexpr int kMediumMaxLen = 16384;       // batches with max_len <= this: one CTA per row, several per SM
 
 // ---------------------------------------------------------------- workspace
 // All offsets are multiples of 256 bytes.
@@ -48,7 +49,8 @@ struct Header {
   int32_t plan_error;   // nonzero when the plan could not be built
   int32_t n_implicit;   // single rows handed out statically (one per idle CTA)
   int32_t dyn_period;   // claims of the ticket counter per call
-  int32_t pad0[4];
+  unsigned long long med_ticket;  // row ticket counter of the medium-row path (0 after a plan)
+  int32_t pad0[2];
   unsigned long long steal;  // single-row ticket counter (advances by dyn_period per call)
   int32_t pad1[14];
   // First expired bounded wait (written once per plan, for diagnosis): kind

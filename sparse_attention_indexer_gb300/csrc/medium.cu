@@ -1,0 +1,422 @@
+// Select + page-table kernel for batches of medium rows (GB300, sm_103a).
+//
+// "Serving GLM5.2 NVFP4 Agentic Workload with SGLang", "Kernel Optimization > TopK-V2":
+// rows are binned by length into a register-resident path, a single-CTA streaming
+// path and a multi-CTA path; "What's next" names ragged top-k for prefill, where
+// thousands of query rows of a few thousand keys each come in one batch. A batch whose
+// rows are all at most kMediumMaxLen values runs here: one 256-thread CTA per row, the
+// row's scores in shared memory, and several CTAs per SM (three for rows of 12K
+// values), so that the latency chains of different rows overlap on one SM.
+//
+// Per row, an exact radix selection over levels of digits, most significant first:
+// the 12-bit coarse digit of the score, then the four bytes of the order-preserving
+// 32-bit key, then the position in two 7-bit halves (smaller positions rank first).
+// At each level the CTA histograms the digit over the values still in the running,
+// finds the boundary digit (fewer than `need` values above it, at least `need` at or
+// above it), emits every value above it, and keeps the boundary digit's values for
+// the next level; a level whose boundary digit holds exactly what is still needed
+// emits them too and ends the row. Key bytes on which every value of the row agrees
+// are skipped. Once few values remain they are kept in a position list, so later
+// levels do not rescan the row. Values are emitted through warp-aggregated shared
+// counters (the order of a row's entries is unspecified) and translated to slots on
+// the way out.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "keys.cuh"
+
+namespace topk {
+
+namespace {
+
+constexpr int kMedThreads = 256;
+constexpr int kMedWarps = kMedThreads / 32;
+constexpr int kCoarseBins = 4096;
+constexpr int kCandCap = 2048;  // running positions kept in a list once this few remain
+constexpr int kLevels = 7;      // coarse digit, 4 key bytes, 2 position halves
+
+// The histogram of levels after the first uses hist[0, 256); the two running-position
+// lists live in hist[256, ...), which the coarse level no longer needs once its
+// boundary is known. Emitted positions are staged in outp and translated to slots in
+// one pass at the end of the row, so that their table reads are in flight together.
+struct MedShared {
+  int hist[kCoarseBins];
+  uint16_t outp[TOPK_MAX_K];
+  int emitted;    // entries written to the row's output
+  int listed;     // positions appended to the next list
+  int bnd_digit;  // boundary digit of the current level
+  int bnd_above;  // running values above it
+  int bnd_at;     // running values at it
+  int status;     // slot errors of the row
+  unsigned key_and, key_or;
+  int warp_tot[kMedWarps];
+};
+static_assert((kCoarseBins - 256) * sizeof(int) >= 2 * kCandCap * sizeof(uint16_t),
+              "the position lists fit the coarse histogram's upper bins");
+
+__device__ __forceinline__ uint16_t* med_list(MedShared& S, int which) {
+  return reinterpret_cast<uint16_t*>(S.hist + 256) + which * kCandCap;
+}
+
+static_assert(kMediumMaxLen <= 1 << 14, "positions fit the two 7-bit position levels and uint16 lists");
+static_assert(kMediumMaxLen <= 64 * kMedThreads, "a thread's entries of a row fit one 64-bit mask");
+
+// Slots of the row's kr staged positions (outp, or the positions 0 .. kr - 1 when
+// `identity`), written with the positions; eight table reads per thread in flight.
+__device__ __forceinline__ void med_translate(const SelectParams& P, MedShared& S, int32_t* os,
+                                              int32_t* op, int t, int kr, bool identity) {
+  for (int o0 = 0; o0 < kr; o0 += 8 * kMedThreads) {
+    int pp[8];
+    int32_t pg[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int o = o0 + j * kMedThreads + (int)threadIdx.x;
+      pp[j] = o < kr ? (identity ? o : (int)S.outp[o]) : -1;
+      pg[j] = pp[j] >= 0 ? __ldg(P.table + (int64_t)t * P.table_ld + pp[j] / P.page_size) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int o = o0 + j * kMedThreads + (int)threadIdx.x;
+      if (pp[j] < 0) continue;
+      const int64_t sl = (int64_t)pg[j] * P.page_size + pp[j] % P.page_size;
+      int32_t v = (int32_t)sl;
+      if (pg[j] < 0) {
+        atomicOr(&S.status, TOPK_STATUS_TABLE_ENTRY);
+        v = -1;
+      } else if (sl > 0x7FFFFFFFll) {
+        atomicOr(&S.status, TOPK_STATUS_SLOT_OVERFLOW);
+        v = -1;
+      }
+      os[o] = v;
+      if (op) op[o] = pp[j];
+    }
+  }
+}
+
+// Digit of level lv: 0 = coarse (4096 bins), 1..4 = key bytes from the top (256
+// bins), 5..6 = position bits 13..7 and 6..0, inverted so that smaller positions rank
+// higher (128 bins).
+__device__ __forceinline__ uint32_t med_digit(int lv, float x, uint32_t key, int p) {
+  if (lv == 0) return coarse_digit(x);
+  if (lv <= 4) return (key >> (32 - 8 * lv)) & 0xFFu;
+  return 127u - (((uint32_t)p >> (lv == 5 ? 7 : 0)) & 127u);
+}
+
+__device__ __forceinline__ int med_bins(int lv) { return lv == 0 ? kCoarseBins : lv <= 4 ? 256 : 128; }
+
+// Boundary digit of the histogram S.hist[0, nb): the digit d with (running values
+// above d) < need <= (values at or above d). Thread t scans bins [t * per, ...) from
+// the top; the block adds up the ranges above each thread.
+__device__ void med_boundary(MedShared& S, int nb, int need) {
+  const int per = (nb + kMedThreads - 1) / kMedThreads;
+  const int lo = min(nb, (int)threadIdx.x * per), hi = min(nb, lo + per);
+  int mine = 0;
+  for (int i = lo; i < hi; ++i) mine += S.hist[i];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = mine;  // sum over lanes [lane, 31] of this warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) S.warp_tot[warp] = incl;
+  __syncthreads();
+  int above = incl - mine;
+  for (int w = warp + 1; w < kMedWarps; ++w) above += S.warp_tot[w];
+  if (above < need && above + mine >= need) {
+    for (int i = hi - 1; i >= lo; --i) {
+      const int c = S.hist[i];
+      if (above + c >= need) {
+        S.bnd_digit = i;
+        S.bnd_above = above;
+        S.bnd_at = c;
+        break;
+      }
+      above += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Class of running-set entry i at level lv: 1 = emitted (above the boundary digit d,
+// or at it when that ends the row), 2 = kept for the next level, 0 = neither or past
+// the set. *pos receives its position.
+__device__ __forceinline__ int med_class(MedShared& S, const float* sx, int src, int n_src, int i,
+                                         int lv, const uint32_t (&chosen)[kLevels], uint32_t d,
+                                         bool ends, bool list, int* pos) {
+  if (i >= n_src) {
+    *pos = 0;
+    return 0;
+  }
+  const int p = src >= 0 ? (int)med_list(S, src)[i] : i;
+  *pos = p;
+  const float x = sx[p];
+  const uint32_t key = f2key(x);
+  if (src < 0)
+    for (int l = 0; l < lv; ++l)
+      if (med_digit(l, x, key, p) != chosen[l]) return 0;
+  const uint32_t dg = med_digit(lv, x, key, p);
+  if (dg > d || (ends && dg == d)) return 1;
+  return list && dg == d ? 2 : 0;
+}
+
+__global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_constant__ SelectParams P) {
+  extern __shared__ __align__(16) unsigned char med_smem[];
+  MedShared& S = *reinterpret_cast<MedShared*>(med_smem);
+  float* const sx = reinterpret_cast<float*>(med_smem + sizeof(MedShared));
+  Header* h = reinterpret_cast<Header*>(P.ws);
+  __shared__ int hdr_ok, row_sh;
+  if (threadIdx.x == 0) {
+    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(h));
+    const int plan_error = __ldcg(&h->plan_error);
+    hdr_ok = ((uint32_t)h0.x == kMagic && h0.y == P.rows && h0.z == P.max_len && plan_error == 0) ? 1 : 0;
+  }
+  const int lane = threadIdx.x & 31;
+  // Rows by tickets. Every call takes exactly rows + gridDim.x of them (each CTA stops
+  // at its first ticket past the rows), so ticket % period numbers the rows of every
+  // call without a reset between calls; the plan sets the counter to 0.
+  const unsigned long long period = (unsigned long long)P.rows + gridDim.x;
+  while (true) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned long long tk = atomicAdd(&h->med_ticket, 1ull);
+      row_sh = (int)(tk % period);
+      S.emitted = 0;
+      S.status = 0;
+      S.key_and = 0xFFFFFFFFu;
+      S.key_or = 0u;
+    }
+    __syncthreads();
+    const int r = row_sh;
+    if (r >= P.rows) break;
+    int32_t* os = P.out_slots + (int64_t)r * P.k;
+    int32_t* op = P.out_pos ? P.out_pos + (int64_t)r * P.k : nullptr;
+    const int L = P.lens[r];
+    int err = 0;
+    if (!hdr_ok) err = TOPK_STATUS_PLAN_MISMATCH;
+    else if (L < 0 || L > P.max_len) err = TOPK_STATUS_LEN;
+    else if (ceil_div64(L, P.page_size) > P.table_ld) err = TOPK_STATUS_TABLE_WIDTH;
+    const int kr = err ? 0 : min(P.k, L);
+    if (err && threadIdx.x == 0) atomicOr(&h->status, err);
+    for (int i = kr + threadIdx.x; i < P.k; i += kMedThreads) {  // -1 padding
+      os[i] = -1;
+      if (op) op[i] = -1;
+    }
+    if (kr == 0) continue;
+    const int t = P.row_to_table ? P.row_to_table[r] : r;
+
+    if (L <= P.k) {  // every position is taken: the scores are not read
+      med_translate(P, S, os, op, t, kr, true);
+      __syncthreads();
+      if (threadIdx.x == 0 && S.status) atomicOr(&h->status, S.status);
+      continue;
+    }
+
+    // Load the row into shared memory; histogram the coarse digit; AND / OR the keys.
+    for (int i = threadIdx.x; i < kCoarseBins; i += kMedThreads) S.hist[i] = 0;
+    __syncthreads();
+    const float* row = P.scores + (int64_t)r * P.ld;
+    int head = 0;  // scalar positions start here
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+      // 16-byte vectors, four per thread in flight before any is used
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      const int nv = L >> 2;
+      for (int i0 = 0; i0 < nv; i0 += 4 * kMedThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * kMedThreads + (int)threadIdx.x;
+          if (i < nv) v[j] = __ldg(r4 + i);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * kMedThreads + (int)threadIdx.x;
+          if (i >= nv) continue;
+          reinterpret_cast<float4*>(sx)[i] = v[j];
+          const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            atomicAdd(&S.hist[coarse_digit(e[c])], 1);
+          }
+        }
+      }
+      head = nv << 2;
+    }
+    for (int p0 = head; p0 < L; p0 += 8 * kMedThreads) {  // the rest: scalars, 8 in flight
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int p = p0 + j * kMedThreads + (int)threadIdx.x;
+        if (p < L) x[j] = __ldg(row + p);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int p = p0 + j * kMedThreads + (int)threadIdx.x;
+        if (p >= L) continue;
+        sx[p] = x[j];
+        atomicAdd(&S.hist[coarse_digit(x[j])], 1);
+      }
+    }
+    __syncthreads();
+    // AND / OR of the keys of the coarse boundary bin's values (filled on the coarse
+    // level): key bytes on which they all agree need no level of their own
+    uint32_t key_and = 0u, key_diff = 0xFFFFFFFFu;
+
+    // Levels. The running set is { p : digit_l(p) == chosen[l] for every level l before
+    // the current one }; src >= 0 when it is listed in med_list(S, src)[0 .. n_src).
+    uint32_t chosen[kLevels];
+    int need = kr, src = -1, n_src = L;
+    for (int lv = 0; lv < kLevels && need > 0; ++lv) {
+      if (lv >= 1 && lv <= 4 && ((key_diff >> (32 - 8 * lv)) & 0xFFu) == 0u) {
+        chosen[lv] = (key_and >> (32 - 8 * lv)) & 0xFFu;  // every running value agrees here
+        continue;
+      }
+      const int nb = med_bins(lv);
+      if (lv > 0) {  // histogram of this level's digit over the running set
+        for (int i = threadIdx.x; i < nb; i += kMedThreads) S.hist[i] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n_src; i += kMedThreads) {
+          const int p = src >= 0 ? (int)med_list(S, src)[i] : i;
+          const float x = sx[p];
+          const uint32_t key = f2key(x);
+          bool run = true;
+          if (src < 0)
+            for (int l = 0; l < lv && run; ++l) run = med_digit(l, x, key, p) == chosen[l];
+          if (run) atomicAdd(&S.hist[med_digit(lv, x, key, p)], 1);
+        }
+        __syncthreads();
+      }
+      med_boundary(S, nb, need);
+      const uint32_t d = (uint32_t)S.bnd_digit;
+      const int above = S.bnd_above, at = S.bnd_at;
+      const bool ends = above + at == need;  // the boundary digit completes the row
+      const bool list = !ends && at <= kCandCap;
+      const int dst = src == 0 ? 1 : 0;
+      if (threadIdx.x == 0) S.listed = 0;
+      __syncthreads();
+      // Emit the running values above the boundary (and at it when that ends the row);
+      // list the values at it for the next level. The first walk classifies this
+      // thread's entries into two bit masks and the warp claims its output ranges with
+      // one shared atomic each (same-address shared atomics from many warps, one per
+      // step, would serialise); the second walk writes at ballot-prefix offsets. On the
+      // coarse level with the boundary on the positive side, the bin's float bounds are
+      // exact and classification is two compares.
+      const bool fast = lv == 0 && d >= 2048u;
+      const float t_at = skip_below(d), t_above = d < 4095u ? skip_below(d + 1u) : 0.0f;
+      uint64_t m_take = 0ull, m_keep = 0ull;
+      uint32_t kand = 0xFFFFFFFFu, kor = 0u;  // keys of the coarse boundary bin's values
+      int j = 0;
+      for (int i0 = 0; i0 < n_src; i0 += kMedThreads, ++j) {
+        int cls = 0;
+        const int i = i0 + (int)threadIdx.x;
+        if (fast) {
+          if (i < n_src) {
+            const float x = sx[i];
+            const bool above_bin = d < 4095u && x >= t_above;
+            const bool at_bin = !above_bin && x >= t_at;
+            cls = above_bin || (ends && at_bin) ? 1 : (list && at_bin ? 2 : 0);
+            if (at_bin) {
+              const uint32_t key = f2key(x);
+              kand &= key;
+              kor |= key;
+            }
+          }
+        } else {
+          int p;
+          cls = med_class(S, sx, src, n_src, i, lv, chosen, d, ends, list, &p);
+        }
+        m_take |= (uint64_t)(cls == 1) << j;
+        m_keep |= (uint64_t)(cls == 2) << j;
+      }
+      if (fast) {
+        kand = __reduce_and_sync(0xffffffffu, kand);
+        kor = __reduce_or_sync(0xffffffffu, kor);
+        if (lane == 0) {
+          atomicAnd(&S.key_and, kand);
+          atomicOr(&S.key_or, kor);
+        }
+      }
+      // each thread writes its own entries at offsets from a warp scan and one shared
+      // atomic per warp (order inside a row is free)
+      const int c_take = __popcll(m_take), c_keep = __popcll(m_keep);
+      const int s_take = warp_incl_scan(c_take), s_keep = warp_incl_scan(c_keep);
+      int o_base = 0, c_base = 0;
+      if (lane == 31) {
+        if (s_take) o_base = atomicAdd(&S.emitted, s_take);
+        if (s_keep) c_base = atomicAdd(&S.listed, s_keep);
+      }
+      int o = __shfl_sync(0xffffffffu, o_base, 31) + s_take - c_take;
+      int c = __shfl_sync(0xffffffffu, c_base, 31) + s_keep - c_keep;
+      for (uint64_t m = m_take | m_keep; m; m &= m - 1) {
+        const int js = __ffsll((long long)m) - 1;
+        const int i = js * kMedThreads + (int)threadIdx.x;
+        const int p = src >= 0 ? (int)med_list(S, src)[i] : i;
+        if ((m_take >> js) & 1ull) {
+          if (o < kr) S.outp[o] = (uint16_t)p;  // o < kr by construction; guarded
+          ++o;
+        } else {
+          med_list(S, dst)[c++] = (uint16_t)p;
+        }
+      }
+      if (fast) {
+        __syncthreads();
+        key_and = S.key_and;
+        key_diff = S.key_and ^ S.key_or;
+      }
+      __syncthreads();
+      chosen[lv] = d;
+      need = ends ? 0 : need - above;
+      if (list) {
+        src = dst;
+        n_src = at;
+      } else {
+        src = -1;
+        n_src = L;
+      }
+    }
+    __syncthreads();
+    med_translate(P, S, os, op, t, min(S.emitted, kr), false);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int st = S.status;
+      if (S.emitted != kr) st |= TOPK_STATUS_ORDER;  // cannot happen: every position is distinct
+      if (st) atomicOr(&h->status, st);
+    }
+  }
+}
+
+}  // namespace
+
+int medium_max_len() { return kMediumMaxLen; }
+
+// Dynamic shared memory of a launch for rows of at most max_len values.
+static size_t medium_smem(int max_len) {
+  return sizeof(MedShared) + (size_t)((max_len + 3) & ~3) * sizeof(float);
+}
+
+cudaError_t launch_medium(const SelectParams& p, int sms, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = medium_smem(p.max_len);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(medium_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)medium_smem(kMediumMaxLen));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, medium_kernel, kMedThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int grid = (int)std::min<int64_t>((int64_t)p.rows, (int64_t)per_sm * sms);
+  if (grid < 1) return cudaSuccess;
+  medium_kernel<<<grid, kMedThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace topk

@@ -377,6 +377,7 @@ __device__ bool plan_small(const int32_t* __restrict__ lens, int rows, int max_l
         h->n_implicit = n_implicit;
         h->dyn_period = n_single - n_implicit + grid;
         h->steal = 0ull;
+        h->med_ticket = 0ull;
         for (int i = 0; i < 8; ++i) h->diag[i] = 0;
         s.bcast[0] = n_multi;
         s.bcast[1] = total_slots;
@@ -764,6 +765,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     h->n_implicit = n_implicit;
     h->dyn_period = n_single - n_implicit + grid;
     h->steal = 0ull;
+    h->med_ticket = 0ull;
     for (int i = 0; i < 8; ++i) h->diag[i] = 0;
   }
   TOPK_MARK(g_plan_trace, 5);
@@ -778,8 +780,9 @@ extern "C" int topk_trace_plan(uint64_t* host, int n) {
 }
 #endif
 
-// Plan of a batch of short rows (max_len <= kShortMaxLen, the register path: one warp
-// per row, no work list): the header alone, which the select kernel checks.
+// Plan of a batch of short or medium rows (max_len <= kMediumMaxLen: the register path,
+// one warp per row, or the medium path, one CTA per row; no work list): the header
+// alone, which the select kernels check, with the medium path's row tickets at 0.
 __global__ void short_plan_kernel(int rows, int max_len, int grid, char* ws) {
   if (threadIdx.x != 0) return;
   Header* h = reinterpret_cast<Header*>(ws);
@@ -795,12 +798,14 @@ __global__ void short_plan_kernel(int rows, int max_len, int grid, char* ws) {
   h->plan_error = 0;
   h->n_implicit = 0;
   h->dyn_period = 0;
+  h->steal = 0ull;
+  h->med_ticket = 0ull;
   for (int i = 0; i < 8; ++i) h->diag[i] = 0;
 }
 
 cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, int chunk_force,
                         void* ws, cudaStream_t stream) {
-  if (max_len <= kShortMaxLen && chunk_force == 0) {
+  if (max_len <= kMediumMaxLen && chunk_force == 0) {
     short_plan_kernel<<<1, 32, 0, stream>>>(rows, max_len, grid, static_cast<char*>(ws));
     return cudaGetLastError();
   }
@@ -821,7 +826,7 @@ cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, in
 int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_force, char* ws) {
   const Layout lay = make_layout(rows);
   Header* h = reinterpret_cast<Header*>(ws + lay.header);
-  if (max_len <= kShortMaxLen && chunk_force == 0) {  // the register path: header only
+  if (max_len <= kMediumMaxLen && chunk_force == 0) {  // register or medium path: header only
     *h = Header{};
     h->magic = kMagic;
     h->rows = rows;
@@ -949,6 +954,7 @@ int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_fo
   h->n_implicit = n_implicit;
   h->dyn_period = n_single - n_implicit + grid;
   h->steal = 0ull;
+  h->med_ticket = 0ull;
   for (int i = 0; i < 8; ++i) h->diag[i] = 0;
   return plan_error;
 }

@@ -153,9 +153,11 @@ def test_special_values():
     lens = np.array([L, L - 1, L - 2, L - 3, 5000, 2049, 2048, 1], np.int32)
     tab = np.stack([rng.permutation(-(-L // 64)).astype(np.int32) for _ in rows])
     b = W.Batch("special", s, lens, L, 2048, tab, None, 64)
-    for chunk in (0, 256):
+    # planned with a max_len above the medium range, so that a forced chunk splits rows
+    wide = dataclasses.replace(W.with_ld(b, 16392), max_len=16385)
+    for bb, chunk in ((b, 0), (wide, 0), (wide, 256)):
         for k in (1, 2, 2048):
-            slots, pos, st = run_gpu(b, k=k, chunk=chunk)
+            slots, pos, st = run_gpu(bb, k=k, chunk=chunk)
             assert st == 0
             compare_with_oracle(b, k, slots, pos)
 
@@ -226,8 +228,11 @@ def test_device_plan_matches_host_reference():
                      [48_128 * 21] * 7, [48_127] * 32, [200_000] * 50, [48_127] * 64,
                      [3000 + 977 * i for i in range(63)], spread(500), spread(700),
                      err_rows)]
+    pf = W.prefill()
+    # the medium batches on the full planner: a max_len above the medium range
+    wide = [types.SimpleNamespace(lens=x.lens, rows=x.rows, max_len=16385) for x in (W.pr1(), pf)]
     for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, more,
-              W.tiny_rows()[0], W.tiny_rows()[15], W.prefill(), *big):
+              W.tiny_rows()[0], W.tiny_rows()[15], pf, *wide, *big):
         lens = torch.from_numpy(b.lens).cuda()
         core = PagedTopK(b.rows, b.max_len)
         core.plan(lens)
@@ -236,7 +241,7 @@ def test_device_plan_matches_host_reference():
         B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img_host)
         hd, rd, sd, (fd, ud), info = parse_plan(img_dev, b.rows)
         hh, rh, sh, (fh, uh), _ = parse_plan(img_host, b.rows)
-        if b.max_len <= 256:  # register path: the plan is its header alone
+        if b.max_len <= 16384:  # register or medium path: the plan is its header alone
             assert hd == hh
             continue
         if b.rows == len(err_rows) and b.max_len > 48_128:
@@ -281,7 +286,10 @@ def test_status_errors():
 
 
 def test_plan_mismatch_is_reported():
-    b = W.pr1()
+    """A full plan records every row's length; a select with other lengths reports the
+    mismatch. (Plans of the register and medium paths are the header alone: they hold
+    no lengths, and any lengths up to max_len are served exactly.)"""
+    b = dataclasses.replace(W.with_ld(W.pr1(), 16388), max_len=16385)
     scores, lens, table, r2t = to_dev(b)
     core = PagedTopK(b.rows, b.max_len)
     core.plan(lens)

@@ -18,7 +18,8 @@ S = pytest.importorskip("sparse_attention_indexer_gb300")
 B = S.binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SHORT_MAX_LEN = 256  # batches whose rows are at most this long take the register path
+HEADER_ONLY_MAX_LEN = 16384  # batches of rows at most this long: register or medium path
+ABOVE_MEDIUM = HEADER_ONLY_MAX_LEN + 1  # a max_len that keeps a batch on the full planner
 
 
 def _lib_or_skip():
@@ -76,8 +77,9 @@ def check_plan(lens, max_len, grid, chunk=0):
     counts one claim per remaining single row plus one failing claim per CTA."""
     _lib_or_skip()
     hdr, ri, singles, (first, units), info = host_plan(lens, max_len, grid, chunk)
-    if max_len <= SHORT_MAX_LEN and chunk == 0:
-        # register path (one warp per row): the plan is its header alone
+    if max_len <= HEADER_ONLY_MAX_LEN and chunk == 0:
+        # register path (one warp per row) or medium path (one CTA per row): the plan is
+        # its header alone
         assert hdr["magic"] == 0x54504B32 and hdr["rows"] == len(lens)
         assert hdr["max_len"] == max_len and hdr["status"] == 0 and hdr["plan_error"] == 0
         assert hdr["waves"] == 0 and hdr["n_multi"] == 0 and hdr["n_single"] == len(lens)
@@ -160,8 +162,11 @@ def test_plan_80k_spreads_rows_over_the_grid():
 
 
 def test_plan_all_workloads():
-    for b in [W.pr1(), W.mixed_decode(), W.adversarial()] + W.tiny_rows()[:3]:
+    for b in [W.pr1(), W.mixed_decode(), W.adversarial(), W.prefill()] + W.tiny_rows()[:3]:
         check_plan(b.lens, b.max_len, 152)
+    # the medium batches on the full planner (a max_len above the medium range)
+    for b in (W.pr1(), W.prefill()):
+        check_plan(b.lens, ABOVE_MEDIUM, 152)
 
 
 @pytest.mark.parametrize("chunk", [16, 64, 1000, 4096, 48128])
@@ -175,10 +180,12 @@ def test_plan_forced_chunks(chunk):
 
 
 def test_plan_degenerate_lengths():
-    check_plan(np.array([0, 0, 0], np.int32), 300, 152)
-    check_plan(np.array([-5, 301, 50], np.int32), 300, 152)  # invalid lengths become single rows
-    check_plan(np.array([], np.int32).reshape(0), 300, 152)
+    M = ABOVE_MEDIUM
+    check_plan(np.array([0, 0, 0], np.int32), M, 152)
+    check_plan(np.array([-5, M + 1, 50], np.int32), M, 152)  # invalid lengths become single rows
+    check_plan(np.array([], np.int32).reshape(0), M, 152)
     check_plan(np.array([-5, 101, 50], np.int32), 100, 152)  # register path: header only
+    check_plan(np.array([-5, 5001, 50], np.int32), 5000, 152)  # medium path: header only
     check_plan(np.array([0, 0, 0], np.int32), 100, 152, chunk=16)  # forced: full plan
     rng = np.random.default_rng(3)
     lens = rng.integers(0, 300_000, size=400).astype(np.int32)
