@@ -37,6 +37,7 @@ constexpr int kMedWarps = kMedThreads / 32;
 constexpr int kCoarseBins = 4096;
 constexpr int kCandCap = 2048;  // running positions kept in a list once this few remain
 constexpr int kLevels = 7;      // coarse digit, 4 key bytes, 2 position halves
+constexpr int kFinishPer = 8;   // values per lane of the one-warp finish (256 in all)
 
 // The histogram of levels after the first uses hist[0, 256); the two running-position
 // lists live in hist[256, ...), which the coarse level no longer needs once its
@@ -54,6 +55,7 @@ struct MedShared {
   unsigned key_and, key_or;
   int warp_tot[kMedWarps];
 };
+static_assert(sizeof(MedShared) % 16 == 0, "the row buffer after it is 16-byte aligned");
 static_assert((kCoarseBins - 256) * sizeof(int) >= 2 * kCandCap * sizeof(uint16_t),
               "the position lists fit the coarse histogram's upper bins");
 
@@ -114,7 +116,8 @@ __device__ void med_boundary(MedShared& S, int nb, int need) {
   const int per = (nb + kMedThreads - 1) / kMedThreads;
   const int lo = min(nb, (int)threadIdx.x * per), hi = min(nb, lo + per);
   int mine = 0;
-  for (int i = lo; i < hi; ++i) mine += S.hist[i];
+  // lanes read their ranges in rotated order, so one load touches distinct banks
+  for (int i = 0; i < hi - lo; ++i) mine += S.hist[lo + ((i + (int)threadIdx.x) % (hi - lo))];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = mine;  // sum over lanes [lane, 31] of this warp
 #pragma unroll
@@ -139,6 +142,88 @@ __device__ void med_boundary(MedShared& S, int nb, int need) {
     }
   }
   __syncthreads();
+}
+
+// One warp selects the `need` best of the n listed positions (n <= 32 * kFinishPer):
+// lane l holds positions list[l + 32 c] as 64-bit composite keys (score key << 14 |
+// 16383 - position, all distinct), and a radix selection runs from the highest bit
+// where they differ, one warp-wide count per bit. The selected positions are appended
+// to S.outp after the S.emitted already there.
+__device__ void med_warp_finish(MedShared& S, const float* sx, const uint16_t* list, int n, int need,
+                                int kr) {
+  const int lane = threadIdx.x & 31;
+  uint64_t key[kFinishPer];
+  int pos[kFinishPer];
+  uint32_t cand = 0u;
+  uint32_t an_hi = 0xFFFFFFFFu, an_lo = 0xFFFFFFFFu, or_hi = 0u, or_lo = 0u;
+#pragma unroll
+  for (int c = 0; c < kFinishPer; ++c) {
+    const int i = lane + 32 * c;
+    key[c] = 0ull;
+    pos[c] = 0;
+    if (i < n) {
+      pos[c] = list[i];
+      key[c] = ((uint64_t)f2key(sx[pos[c]]) << 14) | (uint64_t)(16383 - pos[c]);
+      cand |= 1u << c;
+      an_hi &= (uint32_t)(key[c] >> 32);
+      an_lo &= (uint32_t)key[c];
+      or_hi |= (uint32_t)(key[c] >> 32);
+      or_lo |= (uint32_t)key[c];
+    }
+  }
+  an_hi = __reduce_and_sync(0xffffffffu, an_hi);
+  an_lo = __reduce_and_sync(0xffffffffu, an_lo);
+  or_hi = __reduce_or_sync(0xffffffffu, or_hi);
+  or_lo = __reduce_or_sync(0xffffffffu, or_lo);
+  const uint64_t diff = ((uint64_t)(an_hi ^ or_hi) << 32) | (uint64_t)(an_lo ^ or_lo);
+  uint32_t sel = 0u;
+  if (diff == 0ull) {
+    sel = cand;  // a single value: it is the one needed
+  } else {
+    for (int bit = 63 - __clzll((long long)diff); bit >= 0 && need > 0; --bit) {
+      uint32_t m1 = 0u;
+#pragma unroll
+      for (int c = 0; c < kFinishPer; ++c) m1 |= (uint32_t)((key[c] >> bit) & 1ull) << c;
+      m1 &= cand;
+      const int cnt = (int)__reduce_add_sync(0xffffffffu, (unsigned)__popc(m1));
+      if (cnt >= need) {
+        cand = m1;
+        if (cnt == need) {
+          sel |= m1;
+          need = 0;
+        }
+      } else {
+        sel |= m1;
+        need -= cnt;
+        cand &= ~m1;
+      }
+    }
+    if (need > 0) sel |= cand;  // the last remaining value (the keys are distinct)
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  int base = S.emitted;
+#pragma unroll
+  for (int c = 0; c < kFinishPer; ++c) {
+    const bool s = (sel >> c) & 1u;
+    const unsigned b = __ballot_sync(0xffffffffu, s);
+    if (s) {
+      const int o = base + __popc(b & lt);
+      if (o < kr) S.outp[o] = (uint16_t)pos[c];  // o < kr by construction; guarded
+    }
+    base += __popc(b);
+  }
+  if (lane == 0) S.emitted = base;
+}
+
+// Bulk prefetch of row r's scores into L2 (whole 16-byte units from an aligned start;
+// an unaligned row is not prefetched).
+__device__ __forceinline__ void med_prefetch_row(const SelectParams& P, int r) {
+  const int L = __ldg(P.lens + r);
+  if (L <= P.k || L > P.max_len) return;
+  const float* row = P.scores + (int64_t)r * P.ld;
+  const uint32_t bytes = (uint32_t)(L * 4) & ~15u;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0 || bytes == 0) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"(bytes) : "memory");
 }
 
 // Class of running-set entry i at level lv: 1 = emitted (above the boundary digit d,
@@ -168,7 +253,7 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
   MedShared& S = *reinterpret_cast<MedShared*>(med_smem);
   float* const sx = reinterpret_cast<float*>(med_smem + sizeof(MedShared));
   Header* h = reinterpret_cast<Header*>(P.ws);
-  __shared__ int hdr_ok, row_sh;
+  __shared__ int hdr_ok, row_sh;  // row_sh: the row this CTA works on
   if (threadIdx.x == 0) {
     const int4 h0 = __ldcg(reinterpret_cast<const int4*>(h));
     const int plan_error = __ldcg(&h->plan_error);
@@ -178,12 +263,17 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
   // Rows by tickets. Every call takes exactly rows + gridDim.x of them (each CTA stops
   // at its first ticket past the rows), so ticket % period numbers the rows of every
   // call without a reset between calls; the plan sets the counter to 0.
+  // Thread 0 claims the next row's ticket at the start of each row and reads it only
+  // after the row's coarse level (then it prefetches that row into L2), so the claim's
+  // round trip stays off the row's path.
   const unsigned long long period = (unsigned long long)P.rows + gridDim.x;
+  unsigned long long pending = 0ull;  // thread 0: the claimed next ticket
+  if (threadIdx.x == 0) pending = atomicAdd(&h->med_ticket, 1ull);
   while (true) {
     __syncthreads();
     if (threadIdx.x == 0) {
-      const unsigned long long tk = atomicAdd(&h->med_ticket, 1ull);
-      row_sh = (int)(tk % period);
+      row_sh = (int)(pending % period);
+      if (row_sh < P.rows) pending = atomicAdd(&h->med_ticket, 1ull);
       S.emitted = 0;
       S.status = 0;
       S.key_and = 0xFFFFFFFFu;
@@ -270,6 +360,13 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
     uint32_t chosen[kLevels];
     int need = kr, src = -1, n_src = L;
     for (int lv = 0; lv < kLevels && need > 0; ++lv) {
+      if (src >= 0 && n_src <= 32 * kFinishPer) {
+        // few values left, listed: one warp selects `need` of them in registers
+        if (threadIdx.x < 32) med_warp_finish(S, sx, med_list(S, src), n_src, need, kr);
+        __syncthreads();
+        need = 0;
+        break;
+      }
       if (lv >= 1 && lv <= 4 && ((key_diff >> (32 - 8 * lv)) & 0xFFu) == 0u) {
         chosen[lv] = (key_and >> (32 - 8 * lv)) & 0xFFu;  // every running value agrees here
         continue;
@@ -290,6 +387,10 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
         __syncthreads();
       }
       med_boundary(S, nb, need);
+      if (lv == 0 && threadIdx.x == 0) {
+        const int nx = (int)(pending % period);
+        if (nx < P.rows) med_prefetch_row(P, nx);
+      }
       const uint32_t d = (uint32_t)S.bnd_digit;
       const int above = S.bnd_above, at = S.bnd_at;
       const bool ends = above + at == need;  // the boundary digit completes the row
@@ -308,28 +409,40 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       const float t_at = skip_below(d), t_above = d < 4095u ? skip_below(d + 1u) : 0.0f;
       uint64_t m_take = 0ull, m_keep = 0ull;
       uint32_t kand = 0xFFFFFFFFu, kor = 0u;  // keys of the coarse boundary bin's values
-      int j = 0;
-      for (int i0 = 0; i0 < n_src; i0 += kMedThreads, ++j) {
-        int cls = 0;
-        const int i = i0 + (int)threadIdx.x;
-        if (fast) {
-          if (i < n_src) {
-            const float x = sx[i];
+      if (fast) {
+        // coarse level, boundary on the positive side: four values per step, bit
+        // 4 step + c of the masks for position 4 (step * threads + t) + c
+        const int nv = (L + 3) >> 2;
+        int jb = 0;
+        for (int v0 = 0; v0 < nv; v0 += kMedThreads, jb += 4) {
+          const int v = v0 + (int)threadIdx.x;
+          if (v >= nv) continue;
+          const float4 q = reinterpret_cast<const float4*>(sx)[v];
+          const float e[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float x = 4 * v + c < L ? e[c] : __int_as_float(0xFF800000);  // -inf: below every bin >= 2048
             const bool above_bin = d < 4095u && x >= t_above;
             const bool at_bin = !above_bin && x >= t_at;
-            cls = above_bin || (ends && at_bin) ? 1 : (list && at_bin ? 2 : 0);
+            const int cls = above_bin || (ends && at_bin) ? 1 : (list && at_bin ? 2 : 0);
             if (at_bin) {
               const uint32_t key = f2key(x);
               kand &= key;
               kor |= key;
             }
+            m_take |= (uint64_t)(cls == 1) << (jb + c);
+            m_keep |= (uint64_t)(cls == 2) << (jb + c);
           }
-        } else {
-          int p;
-          cls = med_class(S, sx, src, n_src, i, lv, chosen, d, ends, list, &p);
         }
-        m_take |= (uint64_t)(cls == 1) << j;
-        m_keep |= (uint64_t)(cls == 2) << j;
+      } else {
+        int j = 0;
+        for (int i0 = 0; i0 < n_src; i0 += kMedThreads, ++j) {
+          int p;
+          const int cls = med_class(S, sx, src, n_src, i0 + (int)threadIdx.x, lv, chosen, d, ends,
+                                    list, &p);
+          m_take |= (uint64_t)(cls == 1) << j;
+          m_keep |= (uint64_t)(cls == 2) << j;
+        }
       }
       if (fast) {
         kand = __reduce_and_sync(0xffffffffu, kand);
@@ -353,7 +466,8 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       for (uint64_t m = m_take | m_keep; m; m &= m - 1) {
         const int js = __ffsll((long long)m) - 1;
         const int i = js * kMedThreads + (int)threadIdx.x;
-        const int p = src >= 0 ? (int)med_list(S, src)[i] : i;
+        const int p = fast ? 4 * ((js >> 2) * kMedThreads + (int)threadIdx.x) + (js & 3)
+                           : src >= 0 ? (int)med_list(S, src)[i] : i;
         if ((m_take >> js) & 1ull) {
           if (o < kr) S.outp[o] = (uint16_t)p;  // o < kr by construction; guarded
           ++o;
