@@ -8,7 +8,7 @@
  * logical position into a physical indexer KV-cache slot through a paged block
  * table, in one kernel. A planning kernel bins rows by length and builds a work
  * list once per batch; the plan is reused by every select call (every indexer
- * layer) of that batch.
+ * layer) of that batch (the reuse contract is stated at topk_plan).
  *
  * Readings of what the pages leave open (they define the exact result):
  *   - order: position p ranks before q iff s(p) > s(q), or s(p) == s(q) and p < q;
@@ -88,13 +88,23 @@ int topk_chunk_capacity(void);
 
 /* Planning kernel (one launch). Reads the device-resident lengths lens[rows] (int32,
  * device) and writes the plan into `workspace` (device, 256-byte aligned, at least
- * topk_workspace_bytes(rows, max_len) bytes): every row is binned by length into a
- * path (copy-all for len <= k is decided later, per call), a single-CTA path whose
- * row stays resident in one CTA's shared memory, or a multi-CTA path whose row is
- * split into chunks processed by co-resident CTAs that combine their histograms
- * through global memory. Also resets the workspace counters and the status word.
- * The plan depends only on lens, rows and max_len; it is valid for every k and
- * every score tensor. */
+ * topk_workspace_bytes(rows, max_len) bytes). The batch's max_len picks the path:
+ *   - max_len <= 256: one warp per row, the row in registers;
+ *   - max_len <= 16384: one CTA per row, several CTAs per SM, the row in shared memory;
+ *   - otherwise every row is binned by length into a single-CTA path (the row
+ *     resident in one CTA's shared memory) or a multi-CTA path (the row split into
+ *     chunks processed by co-resident CTAs that combine their histograms through
+ *     global memory), and the plan holds that work list.
+ * For the first two paths the plan is its header alone (a forced chunk, see
+ * topk_plan_ex, still builds the work list, which those paths do not read). Rows with
+ * len <= k are copied whole on every path. Also resets the workspace counters and the
+ * status word.
+ *
+ * Reuse: one plan serves every select call on the same rows, max_len and lens, for
+ * any k, scores, block table, row map, page size and outputs; plan again when the
+ * lengths change, and after a call that left a nonzero status. A select whose lens
+ * differ from a work-list plan's reports TOPK_STATUS_PLAN_MISMATCH; header-only plans
+ * record no lengths, and those paths serve any lens up to max_len. */
 int topk_plan(const int32_t* lens, int rows, int max_len, void* workspace,
               size_t ws_bytes, topk_stream_t stream);
 
