@@ -22,7 +22,15 @@
  *     i takes victim i: the victim's old position loses its mapping, the slot maps to
  *     p, hot_step = step, and host row host_base[j] + p is copied into KV row
  *     hot_rows[j][v], which is the resolved row.
- * Steps must increase from call to call; the hot state starts all -1.
+ * Steps never decrease from call to call; the hot state starts all -1.
+ *
+ * Multi-token verify steps (section "Composing with the rest of vLLM": with speculative
+ * decoding the hot buffers hold (num_speculative_tokens + 2) x top-K rows): a request's
+ * query rows (the decoded token and its draft tokens, each with its own top-K) share
+ * its hot state. hisparse_resolve_mtp resolves them one after another at the same
+ * step, as consecutive hisparse_resolve calls with one step value would: a position
+ * an earlier row brought in is a hit for a later row, and a slot any of them used at
+ * this step is not a victim for the rest.
  */
 #ifndef HISPARSE_RESOLVER_H
 #define HISPARSE_RESOLVER_H
@@ -79,6 +87,19 @@ int hisparse_resolve(const int32_t* positions, int rows, int k, const int32_t* b
                      int64_t host_rows, uint8_t* kv, int64_t kv_rows, int row_bytes,
                      int32_t* out_rows, int32_t* counts, int32_t* status,
                      resolver_stream_t stream);
+
+/* The same for q_rows query rows per request (q_rows >= 1): positions and out_rows
+ * are [rows, q_rows, k]; request j's rows are resolved in order q = 0 .. q_rows - 1 at
+ * step `step`, by the request's one CTA; counts sum over its rows. Other arguments,
+ * return codes and status bits as hisparse_resolve (RESOLVER_ERR_SHAPE also for
+ * q_rows < 1). */
+int hisparse_resolve_mtp(const int32_t* positions, int rows, int q_rows, int k,
+                         const int32_t* block_table, int64_t table_ld, int page_size,
+                         int32_t* token_to_hot, int64_t map_ld, int32_t* hot_token,
+                         int32_t* hot_step, const int32_t* hot_rows, int hot_size, int step,
+                         const uint8_t* host_kv, const int64_t* host_base, int64_t host_rows,
+                         uint8_t* kv, int64_t kv_rows, int row_bytes, int32_t* out_rows,
+                         int32_t* counts, int32_t* status, resolver_stream_t stream);
 
 #ifdef __cplusplus
 }

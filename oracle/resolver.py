@@ -122,3 +122,27 @@ def resolve_step(positions, block_table, page_size, token_to_hot, hot_token, hot
             out[j, i] = hot_rows[j, v]
             counts[j, 2] += 1
     return out, counts, err
+
+
+def resolve_mtp_step(positions, block_table, page_size, token_to_hot, hot_token, hot_step,
+                     hot_rows, step, host_kv, host_base, kv, mutant=0):
+    """One multi-token verify step: positions [rows, q_rows, k]; request j's query rows
+    q = 0 .. q_rows - 1 (the decoded token and its draft tokens, each with its own
+    top-K) share its hot state and are resolved one after another at the same step
+    (reading: the pages size hot buffers for this case at (num_speculative_tokens + 2)
+    x top-K, section "Composing with the rest of vLLM", and leave the order open; the
+    plainest reading is that of consecutive single-row steps with one step value).
+    Returns (rows resolved [rows, q_rows, k], counts [rows, 3] summed over the query
+    rows, status bits)."""
+    pos = np.asarray(positions, np.int64)
+    R, Q, K = pos.shape
+    out = np.full((R, Q, K), -1, np.int32)
+    counts = np.zeros((R, 3), np.int32)
+    err = 0
+    for q in range(Q):
+        o, c, e = resolve_step(pos[:, q, :], block_table, page_size, token_to_hot, hot_token,
+                               hot_step, hot_rows, step, host_kv, host_base, kv, mutant)
+        out[:, q, :] = o
+        counts += c
+        err |= e
+    return out, counts, err

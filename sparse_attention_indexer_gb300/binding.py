@@ -33,7 +33,7 @@ EXPORTS = (
     "topk_plan_ex", "topk_select_paged", "topk_read_status", "topk_clear_status",
     "topk_status_str", "topk_grid_size", "topk_plan_host", "topk_layout_info",
     "topk_select_paged_noalloc", "indexer_k_prologue", "hisparse_resolve",
-    "topk_select_paged_test", "indexer_mqa_logits",
+    "topk_select_paged_test", "indexer_mqa_logits", "hisparse_resolve_mtp",
 )
 
 
@@ -75,6 +75,10 @@ _SIGS = {
     "hisparse_resolve": (_c.c_int, [_VP, _c.c_int, _c.c_int, _VP, _c.c_int64, _c.c_int, _VP,
                                     _c.c_int64, _VP, _VP, _VP, _c.c_int, _c.c_int, _VP, _VP,
                                     _c.c_int64, _VP, _c.c_int64, _c.c_int, _VP, _VP, _VP, _VP]),
+    "hisparse_resolve_mtp": (_c.c_int, [_VP, _c.c_int, _c.c_int, _c.c_int, _VP, _c.c_int64,
+                                        _c.c_int, _VP, _c.c_int64, _VP, _VP, _VP, _c.c_int,
+                                        _c.c_int, _VP, _VP, _c.c_int64, _VP, _c.c_int64, _c.c_int,
+                                        _VP, _VP, _VP, _VP]),
 }
 
 # include/hisparse_resolver.h
@@ -304,6 +308,26 @@ def hisparse_resolve(positions, block_table, page_size: int, token_to_hot, hot_t
     rows, k = int(positions.shape[0]), int(positions.shape[1])
     code = lib().hisparse_resolve(
         _ptr(positions), rows, k, _ptr(block_table), int(block_table.stride(0)),
+        int(page_size), _ptr(token_to_hot), int(token_to_hot.stride(0)), _ptr(hot_token),
+        _ptr(hot_step), _ptr(hot_rows), int(hot_rows.shape[1]), int(step),
+        host_kv.data_ptr() or None, _ptr(host_base), int(host_kv.shape[0]), _ptr(kv),
+        int(kv.shape[0]), int(kv.shape[1]), _ptr(out_rows), _ptr(counts), _ptr(status),
+        _stream(stream))
+    if code < 0:
+        raise ResolverError(code)
+    return code
+
+
+def hisparse_resolve_mtp(positions, block_table, page_size: int, token_to_hot, hot_token,
+                         hot_step, hot_rows, step: int, host_kv, host_base, kv, out_rows,
+                         counts=None, status=None, stream=None) -> int:
+    """hisparse_resolve_mtp of include/hisparse_resolver.h: as hisparse_resolve, with
+    positions and out_rows CUDA int32 [rows, q_rows, k]. Argument marshalling only."""
+    if host_kv.is_cuda or (host_kv.numel() and not host_kv.is_pinned()):
+        raise ValueError("host_kv must be pinned host memory")
+    rows, q_rows, k = (int(x) for x in positions.shape)
+    code = lib().hisparse_resolve_mtp(
+        _ptr(positions), rows, q_rows, k, _ptr(block_table), int(block_table.stride(0)),
         int(page_size), _ptr(token_to_hot), int(token_to_hot.stride(0)), _ptr(hot_token),
         _ptr(hot_step), _ptr(hot_rows), int(hot_rows.shape[1]), int(step),
         host_kv.data_ptr() or None, _ptr(host_base), int(host_kv.shape[0]), _ptr(kv),

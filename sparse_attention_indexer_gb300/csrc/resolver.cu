@@ -47,6 +47,7 @@ struct Params {
   int32_t* out;
   int32_t* counts;
   int32_t* status;
+  int q_rows;  // query rows per request, resolved one after another at the same step
 };
 
 struct Smem {
@@ -91,14 +92,18 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   const int j = blockIdx.x;
-  const int32_t* pos = p.positions + (int64_t)j * p.k;
-  int32_t* out = p.out + (int64_t)j * p.k;
   const int32_t* tab = p.table + (int64_t)j * p.table_ld;
   int32_t* t2h = p.t2h + (int64_t)j * p.map_ld;
   int32_t* htok = p.hot_token + (int64_t)j * p.hot;
   int32_t* hstep = p.hot_step + (int64_t)j * p.hot;
   const int32_t* hrows = p.hot_rows + (int64_t)j * p.hot;
-  int err = 0, n_res = 0, n_hit = 0;
+  int err = 0, n_res = 0, n_hit = 0, n_copy = 0;
+  // The request's query rows, one after another: a later row sees the state an earlier
+  // one left (its misses are hits now, and the slots it used, at this step, are not
+  // victims). Global writes of the block are visible to it after each row's barrier.
+  for (int qr = 0; qr < p.q_rows; ++qr) {
+  const int32_t* pos = p.positions + ((int64_t)j * p.q_rows + qr) * p.k;
+  int32_t* out = p.out + ((int64_t)j * p.q_rows + qr) * p.k;
 
   // The slots' last steps (for the victim order) do not depend on the classification:
   // thread t reads those of slots 8t .. 8t + 7 now, and the hits found below are
@@ -106,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   constexpr int kV = kMaxHot / kThreads;
   static_assert(kV == 8, "8 slots per thread: 4-bit counters, 8 counted offsets");
   const int h0 = threadIdx.x * kV;
+  __syncthreads();  // the previous row's shared state is no longer read
   reinterpret_cast<uint2*>(s.hit_slot)[threadIdx.x] = make_uint2(0u, 0u);
   __syncthreads();
   int sv[kV];
@@ -504,12 +510,13 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
       for (int e = 0; e < kC; ++e)
         if (dst[e] >= 0) *reinterpret_cast<uint4*>(p.kv + dst[e]) = v[e];
     }
-  }
-
-  // 6. counts and status (misses copied = assigned copies)
-  if (p.counts || p.status) {
-    int n_copy = 0;
     for (int rr = threadIdx.x; rr < m; rr += kThreads) n_copy += s.copy_src[rr] >= 0 ? 1 : 0;
+  }
+  __syncthreads();  // this row's state writes are seen by the next row
+  }  // query rows
+
+  // 6. counts and status (misses copied = assigned copies), over all query rows
+  if (p.counts || p.status) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int v0 = n_res, v1 = n_hit, v2 = n_copy, v3 = err;
 #pragma unroll
@@ -546,17 +553,13 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
 
 bool aligned(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
 
-}  // namespace
-
-extern "C" int hisparse_resolve(const int32_t* positions, int rows, int k,
-                                const int32_t* block_table, int64_t table_ld, int page_size,
-                                int32_t* token_to_hot, int64_t map_ld, int32_t* hot_token,
-                                int32_t* hot_step, const int32_t* hot_rows, int hot_size, int step,
-                                const uint8_t* host_kv, const int64_t* host_base,
-                                int64_t host_rows, uint8_t* kv, int64_t kv_rows, int row_bytes,
-                                int32_t* out_rows, int32_t* counts, int32_t* status,
-                                resolver_stream_t stream) {
-  if (rows < 0 || k < 1 || k > kMaxK || hot_size < 1 || hot_size > kMaxHot || page_size < 1 ||
+int resolve_launch(const int32_t* positions, int rows, int q_rows, int k, const int32_t* block_table,
+                   int64_t table_ld, int page_size, int32_t* token_to_hot, int64_t map_ld,
+                   int32_t* hot_token, int32_t* hot_step, const int32_t* hot_rows, int hot_size,
+                   int step, const uint8_t* host_kv, const int64_t* host_base, int64_t host_rows,
+                   uint8_t* kv, int64_t kv_rows, int row_bytes, int32_t* out_rows, int32_t* counts,
+                   int32_t* status, resolver_stream_t stream) {
+  if (rows < 0 || q_rows < 1 || k < 1 || k > kMaxK || hot_size < 1 || hot_size > kMaxHot || page_size < 1 ||
       table_ld < 1 || map_ld < 1 || step < 0 || row_bytes < 16 || (row_bytes & 15) ||
       kv_rows < 0 || host_rows < 0)
     return RESOLVER_ERR_SHAPE;
@@ -579,7 +582,35 @@ extern "C" int hisparse_resolve(const int32_t* positions, int rows, int k,
   Params p{positions, rows,     k,        block_table, table_ld,  page_size, token_to_hot,
            map_ld,    hot_token, hot_step, hot_rows,    hot_size,  step,      host_kv,
            host_base, host_rows, kv,       kv_rows,     row_bytes, out_rows,  counts,
-           status};
+           status,    q_rows};
   resolve_kernel<<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? RESOLVER_OK : RESOLVER_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int hisparse_resolve(const int32_t* positions, int rows, int k,
+                                const int32_t* block_table, int64_t table_ld, int page_size,
+                                int32_t* token_to_hot, int64_t map_ld, int32_t* hot_token,
+                                int32_t* hot_step, const int32_t* hot_rows, int hot_size, int step,
+                                const uint8_t* host_kv, const int64_t* host_base,
+                                int64_t host_rows, uint8_t* kv, int64_t kv_rows, int row_bytes,
+                                int32_t* out_rows, int32_t* counts, int32_t* status,
+                                resolver_stream_t stream) {
+  return resolve_launch(positions, rows, 1, k, block_table, table_ld, page_size, token_to_hot,
+                        map_ld, hot_token, hot_step, hot_rows, hot_size, step, host_kv, host_base,
+                        host_rows, kv, kv_rows, row_bytes, out_rows, counts, status, stream);
+}
+
+extern "C" int hisparse_resolve_mtp(const int32_t* positions, int rows, int q_rows, int k,
+                                    const int32_t* block_table, int64_t table_ld, int page_size,
+                                    int32_t* token_to_hot, int64_t map_ld, int32_t* hot_token,
+                                    int32_t* hot_step, const int32_t* hot_rows, int hot_size,
+                                    int step, const uint8_t* host_kv, const int64_t* host_base,
+                                    int64_t host_rows, uint8_t* kv, int64_t kv_rows, int row_bytes,
+                                    int32_t* out_rows, int32_t* counts, int32_t* status,
+                                    resolver_stream_t stream) {
+  return resolve_launch(positions, rows, q_rows, k, block_table, table_ld, page_size, token_to_hot,
+                        map_ld, hot_token, hot_step, hot_rows, hot_size, step, host_kv, host_base,
+                        host_rows, kv, kv_rows, row_bytes, out_rows, counts, status, stream);
 }

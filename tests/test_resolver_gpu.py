@@ -168,3 +168,68 @@ def test_victims_in_a_hot_buffer_of_odd_size(n_miss, never_used):
     state = _crafted_state(b, 30, 30, n_miss, 100, W.SEED_BASE + 79 + n_miss, never_used)
     counts = _one_step_from(b, state, 30)
     assert np.all(counts[:, 2] == n_miss) and np.all(counts[:, 1] == 100)
+
+
+def run_mtp_sequence(b, hot_rows=None):
+    """hisparse_resolve_mtp step by step against the oracle's multi-token step."""
+    dev = torch.device("cuda", 0)
+    hot_rows = b.hot_rows if hot_rows is None else hot_rows
+    R, H = hot_rows.shape
+    map_ld = int(b.lens.max())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    g_t2h = torch.full((R, map_ld), -1, dtype=torch.int32, device=dev)
+    g_ht = torch.full((R, H), -1, dtype=torch.int32, device=dev)
+    g_hs = torch.full((R, H), -1, dtype=torch.int32, device=dev)
+    g_hot_rows, g_tab, g_base = t(hot_rows), t(b.block_table), t(b.host_base)
+    g_kv = t(b.kv_init)
+    host = torch.from_numpy(b.host_kv).pin_memory()
+    o_t2h = np.full((R, map_ld), -1, np.int32)
+    o_ht = np.full((R, H), -1, np.int32)
+    o_hs = np.full((R, H), -1, np.int32)
+    o_kv = b.kv_init.copy()
+    total = np.zeros((R, 3), np.int64)
+    for s, sel in enumerate(b.steps):
+        out = torch.full(sel.shape, -9, dtype=torch.int32, device=dev)
+        counts = torch.zeros((R, 3), dtype=torch.int32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        B.hisparse_resolve_mtp(t(sel), g_tab, b.page_size, g_t2h, g_ht, g_hs, g_hot_rows, s, host,
+                               g_base, g_kv, out, counts=counts, status=status)
+        torch.cuda.synchronize()
+        o_out, o_counts, o_err = RV.resolve_mtp_step(sel, b.block_table, b.page_size, o_t2h, o_ht,
+                                                     o_hs, hot_rows, s, b.host_kv, b.host_base,
+                                                     o_kv)
+        assert int(status.item()) == o_err, f"step {s}: status {int(status.item())} != {o_err}"
+        assert np.array_equal(out.cpu().numpy(), o_out), f"step {s}: resolved rows differ"
+        assert np.array_equal(counts.cpu().numpy(), o_counts), f"step {s}: counts differ"
+        assert np.array_equal(g_t2h.cpu().numpy(), o_t2h), f"step {s}: position map differs"
+        assert np.array_equal(g_ht.cpu().numpy(), o_ht), f"step {s}: slot map differs"
+        assert np.array_equal(g_hs.cpu().numpy(), o_hs), f"step {s}: slot steps differ"
+        assert np.array_equal(g_kv.cpu().numpy(), o_kv), f"step {s}: KV tensor differs"
+        total += o_counts
+    return total
+
+
+def test_mtp_verify_steps():
+    """Four requests, three query rows each (the decoded token and two drafts), k = 512,
+    hot buffers of (3 + 1) * 512 rows: the rows of a step share the request's hot state."""
+    b = W.hisparse_mtp(seed=W.SEED_BASE + 75, reqs=4, k=512, q_rows=3,
+                       lens=[20000, 30000, 5000, 900], n_steps=5)
+    total = run_mtp_sequence(b)
+    assert total[:, 1].sum() > 0 and total[:, 2].sum() > 0
+
+
+def test_mtp_seven_rows_and_an_exhausted_buffer():
+    """Seven query rows (1 + 6 drafts) at k = 256 with hot buffers of 8 * 256 rows, then
+    the same with a quarter of the slots: later rows' misses run out of victims."""
+    b = W.hisparse_mtp(seed=W.SEED_BASE + 76, reqs=3, k=256, q_rows=7, lens=[12000, 6000, 3000],
+                       row_bytes=32, n_steps=4, draft_new=0.4)
+    run_mtp_sequence(b)
+    run_mtp_sequence(b, hot_rows=b.hot_rows[:, :512].copy())
+
+
+def test_mtp_single_row_equals_the_plain_call():
+    """q_rows = 1 is the plain call."""
+    b = W.hisparse(seed=W.SEED_BASE + 77, reqs=3, k=128, lens=[5000, 2000, 700], row_bytes=16,
+                   n_steps=3)
+    import dataclasses
+    run_mtp_sequence(dataclasses.replace(b, steps=[s[:, None, :] for s in b.steps]))

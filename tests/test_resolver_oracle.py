@@ -209,7 +209,99 @@ def pin_closed_forms(mutant=0):
     return None
 
 
-PINS = [pin_golden, pin_heap_reference, pin_invariants, pin_closed_forms]
+def pin_mtp_hand_worked(mutant=0):
+    """One request, pages of 2, positions 0..7 all host-only, three hot slots (KV rows
+    20, 21, 22), slot 2 last used at step 4, slots 0 and 1 never. Step 5 has two query
+    rows: row 0 selects [3, 5], row 1 selects [5, 6, 7].
+      row 0: 3 and 5 miss; victims are the slots unused at step 5, least recently used
+        first, ties to the lower slot: 0 and 1 (step -1) -> 3 in slot 0 (row 20), 5 in
+        slot 1 (row 21);
+      row 1: 5 is a hit (slot 1, row 21); 6 misses and takes the only slot not used at
+        step 5, slot 2 (row 22), evicting its old position 0; 7 misses with no slot
+        left: -1, status 1.
+    Counts over the rows: 0 resident, 1 hit, 3 copied."""
+    tab = np.full((1, 4), -1, np.int32)
+    host = np.array([[10 * p] for p in range(8)], np.uint8)
+    kv = np.zeros((32, 1), np.uint8)
+    t2h = np.full((1, 8), -1, np.int32)
+    t2h[0, 0] = 2
+    ht = np.array([[-1, -1, 0]], np.int32)
+    hs = np.array([[-1, -1, 4]], np.int32)
+    hot_rows = np.array([[20, 21, 22]], np.int32)
+    pos = np.array([[[3, 5, -1], [5, 6, 7]]], np.int32)
+    out, counts, err = RV.resolve_mtp_step(pos, tab, 2, t2h, ht, hs, hot_rows, 5, host,
+                                           np.array([0], np.int64), kv, mutant)
+    want = [[[20, 21, -1], [21, 22, -1]]]
+    if out.tolist() != want or counts.tolist() != [[0, 1, 3]] or err != RV.ERR_NO_VICTIM:
+        return f"rows {out.tolist()} counts {counts.tolist()} status {err}"
+    if ht.tolist() != [[3, 5, 6]] or hs.tolist() != [[5, 5, 5]] or int(t2h[0, 0]) != -1:
+        return f"hot state {ht.tolist()} {hs.tolist()} map of 0: {t2h[0, 0]}"
+    if kv[20, 0] != 30 or kv[21, 0] != 50 or kv[22, 0] != 60:
+        return f"kv rows {kv[20:23, 0].tolist()}"
+    return None
+
+
+def pin_mtp_invariants(mutant=0):
+    """Over a sequence of generated multi-token steps: after each step, every resolved
+    non-resident position of every query row is held by the slot it resolved to, used
+    at this step (no row evicts a slot an earlier row used); each position missing
+    before the step is copied once whatever the number of rows that select it; the slots
+    used at this step are exactly those of the distinct non-resident positions."""
+    b = W.hisparse_mtp(seed=W.SEED_BASE + 900, reqs=2, k=48, q_rows=3, lens=[2500, 800],
+                       tail=128, row_bytes=16, n_steps=5, draft_new=0.3)
+    t2h, ht, hs = (np.full((b.rows, int(b.lens.max())), -1, np.int32),
+                   np.full((b.rows, b.hot_size), -1, np.int32),
+                   np.full((b.rows, b.hot_size), -1, np.int32))
+    kv = b.kv_init.copy()
+    for s, st in enumerate(b.steps):
+        before = t2h.copy()
+        out, counts, err = RV.resolve_mtp_step(st, b.block_table, b.page_size, t2h, ht, hs,
+                                               b.hot_rows, s, b.host_kv, b.host_base, kv, mutant)
+        if err:
+            return f"step {s}: status {err} (the hot buffers hold every row's positions)"
+        for j in range(b.rows):
+            nonres = set()
+            for q in range(st.shape[1]):
+                for i, p in enumerate(st[j, q]):
+                    p = int(p)
+                    if p < 0 or int(b.block_table[j, p // b.page_size]) >= 0:
+                        continue
+                    nonres.add(p)
+                    h = int(t2h[j, p])
+                    if h < 0 or int(b.hot_rows[j, h]) != int(out[j, q, i]) or int(hs[j, h]) != s:
+                        return f"step {s}: row {q} position {p} lost its slot within the step"
+                    if not np.array_equal(kv[out[j, q, i]], b.host_kv[b.host_base[j] + p]):
+                        return f"step {s}: row {out[j, q, i]} does not hold position {p}"
+            missing = sum(1 for p in nonres if int(before[j, p]) < 0)
+            if int(counts[j, 2]) != missing:
+                return f"step {s}: {counts[j, 2]} copies for {missing} missing positions"
+            if int((hs[j] == s).sum()) != len(nonres):
+                return f"step {s}: {(hs[j] == s).sum()} slots used for {len(nonres)} positions"
+    return None
+
+
+def pin_mtp_closed_form(mutant=0):
+    """A step whose query rows all select the same positions resolves like one row, and
+    the later rows are all hits."""
+    b = _small(5, k=40)
+    one = run_steps(b, mutant, steps=[b.steps[0]])[0]
+    t2h, ht, hs = fresh_state(b)
+    kv = b.kv_init.copy()
+    pos = np.stack([b.steps[0]] * 3, axis=1)
+    out, counts, err = RV.resolve_mtp_step(pos, b.block_table, b.page_size, t2h, ht, hs,
+                                           b.hot_rows, 0, b.host_kv, b.host_base, kv, mutant)
+    if any(not np.array_equal(out[:, q], one[0]) for q in range(3)):
+        return "repeated rows resolved to other rows"
+    c1 = one[1]
+    if not np.array_equal(counts, c1 + np.stack([0 * c1[:, 0], 2 * (c1[:, 1] + c1[:, 2]),
+                                                 0 * c1[:, 0]], axis=1) + 2 * np.stack(
+            [c1[:, 0], 0 * c1[:, 0], 0 * c1[:, 0]], axis=1)):
+        return f"counts {counts.tolist()} against one row's {c1.tolist()}"
+    return None
+
+
+PINS = [pin_golden, pin_heap_reference, pin_invariants, pin_closed_forms, pin_mtp_hand_worked,
+        pin_mtp_invariants, pin_mtp_closed_form]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)

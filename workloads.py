@@ -455,6 +455,56 @@ def hisparse(seed: int = SEED_BASE + 7, reqs: int = 8, k: int = 2048, page_size:
                          row_bytes, host_kv, host_base, kv_init, steps)
 
 
+def hisparse_mtp(seed: int = SEED_BASE + 10, reqs: int = 4, k: int = 512, q_rows: int = 3,
+                 page_size: int = 64, lens=None, tail: int = 1024, resident_frac: float = 0.1,
+                 row_bytes: int = 64, n_steps: int = 4, keep: float = 0.85, tail_frac: float = 0.1,
+                 draft_new: float = 0.2):
+    """Multi-token verify steps: each step has q_rows query rows per request (the
+    decoded token and its drafts). Row 0 follows the recipe of `hisparse`; each draft
+    row takes row 0's positions and replaces about `draft_new` of them with other
+    positions of the context (draft tokens attend to much the same tokens). Hot buffers
+    hold (q_rows + 1) * k rows, the pages' (num_speculative_tokens + 2) x top-K."""
+    base = hisparse(seed=seed, reqs=reqs, k=k, page_size=page_size, lens=lens, tail=tail,
+                    resident_frac=resident_frac, row_bytes=row_bytes, n_steps=n_steps,
+                    keep=keep, tail_frac=tail_frac)
+    rng = _rng(seed + 1)
+    R = base.rows
+    H = (q_rows + 1) * k
+    # re-lease hot buffers of H rows per request from fresh blocks after the base pool
+    hot_blocks = -(-H // page_size)
+    first = base.kv_rows // page_size
+    hot_rows = np.zeros((R, H), np.int32)
+    for j in range(R):
+        b0 = first + j * hot_blocks
+        hot_rows[j] = (b0 * page_size + rng.permutation(hot_blocks * page_size)[:H]).astype(np.int32)
+    kv_rows = (first + R * hot_blocks) * page_size
+    kv_init = np.concatenate([base.kv_init, rng.integers(0, 256, size=(kv_rows - base.kv_rows,
+                                                                       row_bytes), dtype=np.uint8)])
+    steps = []
+    for sel0 in base.steps:
+        st = np.full((R, q_rows, k), -1, np.int32)
+        st[:, 0] = sel0
+        for j in range(R):
+            L = int(base.lens[j])
+            m = int((sel0[j] >= 0).sum())
+            for q in range(1, q_rows):
+                row = sel0[j, :m].copy()
+                seen = set(int(x) for x in row)
+                for i in range(m):
+                    if rng.random() < draft_new:
+                        for _ in range(8):
+                            p = int(rng.integers(0, L))
+                            if p not in seen:
+                                seen.discard(int(row[i]))
+                                row[i] = p
+                                seen.add(p)
+                                break
+                st[j, q, :m] = row[rng.permutation(m)]
+        steps.append(st)
+    return dataclasses.replace(base, name="hisparse_mtp", hot_rows=hot_rows, kv_rows=kv_rows,
+                               kv_init=kv_init, steps=steps)
+
+
 # ---------------------------------------------------------------- indexer MQA logits
 @dataclasses.dataclass
 class LogitsBatch:
