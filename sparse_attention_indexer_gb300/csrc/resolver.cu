@@ -88,6 +88,9 @@ __device__ int block_excl_scan(int v, int* total, Smem& s) {
   return before + x - v;
 }
 
+// kRows: the request has several query rows (a loop over them); else exactly one, and
+// the body compiles without the loop (the loop costs the one-row step registers).
+template <bool kRows>
 __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
@@ -101,7 +104,8 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   // The request's query rows, one after another: a later row sees the state an earlier
   // one left (its misses are hits now, and the slots it used, at this step, are not
   // victims). Global writes of the block are visible to it after each row's barrier.
-  for (int qr = 0; qr < p.q_rows; ++qr) {
+  const int n_rows = kRows ? p.q_rows : 1;
+  for (int qr = 0; qr < n_rows; ++qr) {
   const int32_t* pos = p.positions + ((int64_t)j * p.q_rows + qr) * p.k;
   int32_t* out = p.out + ((int64_t)j * p.q_rows + qr) * p.k;
 
@@ -574,7 +578,9 @@ int resolve_launch(const int32_t* positions, int rows, int q_rows, int k, const 
     return RESOLVER_ERR_ALIGN;
   static bool attr_set = false;  // the attribute is per function, process-wide
   if (!attr_set) {
-    if (cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(resolve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(Smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(resolve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(Smem)) != cudaSuccess)
       return RESOLVER_ERR_CUDA;
     attr_set = true;
@@ -583,7 +589,10 @@ int resolve_launch(const int32_t* positions, int rows, int q_rows, int k, const 
            map_ld,    hot_token, hot_step, hot_rows,    hot_size,  step,      host_kv,
            host_base, host_rows, kv,       kv_rows,     row_bytes, out_rows,  counts,
            status,    q_rows};
-  resolve_kernel<<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
+  if (q_rows == 1)
+    resolve_kernel<false><<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
+  else
+    resolve_kernel<true><<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? RESOLVER_OK : RESOLVER_ERR_CUDA;
 }
 
