@@ -394,6 +394,10 @@ __device__ __forceinline__ void load8_cg(const uint32_t* p, uint32_t (&v)[8]) {
   v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
 }
 
+__device__ __forceinline__ float vmax4(const float4& x) {
+  return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+}
+
 // Threshold of the unit's row from the local histogram in s.u.hist. For G > 1 a CTA
 // whose chunk holds at least `need` values first finds its own threshold bin for
 // `need` values; the row's threshold cannot lie below it (the row has at least as
@@ -448,8 +452,14 @@ __device__ bool reduce_and_find(Ctx& c, Unit& u, uint32_t* ghist, int need, int 
 // `need` values lie there, the row's threshold is found exactly. Otherwise every CTA
 // publishes the bins it held back and the row meets once more. Outputs as
 // reduce_and_find; false on timeout.
+//
+// While the first barrier propagates, a CTA whose own bin lies on the positive side
+// (where a bin's lower float bound is exact) marks in *pre bit i each of its vectors
+// v = threadIdx.x + i * kThreads that reaches that bound. When the first round is
+// complete the row's threshold bin is at or above the CTA's own bin, so every vector
+// holding a value at or above the row's threshold is marked; *pre_ok says so.
 __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int& local_above,
-                              int& local_eq) {
+                              int& local_eq, uint32_t& pre, bool& pre_ok) {
   Smem& s = c.s;
   const int need = u.kr;
   const int t = threadIdx.x * 8;
@@ -478,7 +488,17 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
       if ((threadIdx.x & 31) == 0) atomicAdd(&s.bc[30], nw);
     }
 #endif
-    if (!group_sync(c, u, (uint32_t)blocal, nullptr)) return false;
+    const uint32_t seq = group_arrive(c, u, (uint32_t)blocal);
+    if (blocal >= 2048) {
+      const float tl = skip_below((uint32_t)blocal);
+      const float4* b4 = reinterpret_cast<const float4*>(s.buf);
+      uint32_t m = 0u;
+      for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads)
+        m |= vmax4(b4[v]) >= tl ? (1u << i) : 0u;
+      pre = m;
+      pre_ok = true;
+    }
+    if (!group_wait(c, u, seq, nullptr)) return false;
     TOPK_MARK(g_select_trace, 25);
     const int top = s.bc[18];
     if (t + 7 >= blocal) {
@@ -496,6 +516,7 @@ __device__ bool coarse_reduce(Ctx& c, Unit& u, int& b, int& above, int& eq, int&
       for (int j = 0; j < 8; ++j)
         if (loc[j] && t + j < blocal) red_add_u32(&u.gs->hist0[t + j], loc[j]);
       u.blocal = 0;
+      pre_ok = false;
       if (!group_sync(c, u, 0u, nullptr)) return false;
       load8_cg(&u.gs->hist0[t], glob);
       find_threshold(glob, loc, need, s);
@@ -619,10 +640,6 @@ __device__ void histogram_chunk(Ctx& c, Unit& u) {
   if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 11] = global_timer_ns();
 #endif
   __syncthreads();
-}
-
-__device__ __forceinline__ float vmax4(const float4& x) {
-  return fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
 }
 
 // ------------------------------------------------------------- boundary selection
@@ -806,8 +823,8 @@ __device__ void emit_ordered(Ctx& c, const Unit& u, int base, Pred pred) {
 // `emitted` row entries (all values above the threshold bin). For G > 1 every level
 // exchanges per-rank counts so that output offsets are deterministic, and each CTA
 // clears the level histogram once the next barrier shows it has been read.
-__device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, uint32_t fa,
-                                uint32_t fo, int local_eq0) {
+__device__ __noinline__ bool refine_in_place(Ctx c, Unit u, int b0, int need, int emitted,
+                                             uint32_t fa, uint32_t fo, int local_eq0) {
   Smem& s = c.s;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
   bool reset_and_or = u.G > 1;  // cleared by rank 0 after the next barrier
@@ -913,6 +930,155 @@ __device__ bool refine_in_place(Ctx& c, Unit& u, int b0, int need, int emitted, 
   return true;
 }
 
+// ------------------------------------------------------------- out-of-line paths
+//
+// Paths that the common rows never take live in out-of-line functions, so that the
+// common path's instructions stay compact: a kernel whose code was evicted fetches it
+// from memory phase by phase, and interleaved rare code lengthens every such fetch.
+// They take the context and the unit by value so that callers keep theirs in
+// registers.
+
+// Pass 2 when the threshold bin's float bounds are not exact (negative side, the top
+// bin) or the boundary bin is too large for a compact list: every value is classified
+// by its coarse digit. Counts, scans and writes the staging lists like the exact
+// path, leaves the staged counts in s.bc[9] (positions) and s.bc[10] (candidates) and
+// returns this thread's AND / OR of the boundary keys (x, y).
+__device__ __noinline__ uint2 pass2_general(Ctx c, Unit u, int b0, bool all_eq, bool fallback,
+                                            bool stage_cand) {
+  Smem& s = c.s;
+  const float4* b4 = reinterpret_cast<const float4*>(s.buf);
+  const float tlo = skip_below((uint32_t)b0);
+  // classify one value: 0 below, 1 above (staged position), 2 boundary
+  auto klass = [&](float x) -> int {
+    const uint32_t dg = coarse_digit(x);
+    if (dg < (uint32_t)b0) return 0;
+    return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
+  };
+  uint32_t fa = 0xFFFFFFFFu, fo = 0u, hm = 0u;
+  int na = 0, nc = 0;
+  for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) {
+    const float4 x = b4[v];
+    if (vmax4(x) < tlo) continue;
+    const int e0 = 4 * v - u.head;
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+    int a = 0, cd = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + j;
+      if (e < 0 || e >= u.n) continue;
+      const int k = klass(xs[j]);
+      if (k == 1) {
+        ++a;
+      } else if (k == 2) {
+        ++cd;
+        if (fallback) {
+          const uint32_t key = f2key(xs[j]);
+          fa &= key;
+          fo |= key;
+        }
+      }
+    }
+    if (!stage_cand) cd = 0;
+    na += a;
+    nc += cd;
+    hm |= (a + cd) ? (1u << i) : 0u;
+  }
+  int tot_ac;
+  const int off_ac = block_excl_scan(na | (nc << 16), &tot_ac, s);
+  if (threadIdx.x == 0) {
+    s.bc[9] = tot_ac & 0xFFFF;
+    s.bc[10] = tot_ac >> 16;
+  }
+  int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
+  while (hm) {
+    const int i = __ffs(hm) - 1;
+    hm &= hm - 1u;
+    const int v = threadIdx.x + i * kThreads;
+    const float4 x = b4[v];
+    const int p0 = u.s0 + 4 * v - u.head;
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e < 0 || e >= u.n) continue;
+      const int k = klass(xs[j]);
+      if (k == 1) {
+        if (oa < TOPK_MAX_K) s.u.l.elist[oa] = p0 + j;
+        ++oa;
+      } else if (k == 2 && stage_cand) {
+        if (oc < kListCap) {
+          s.u.l.ckey[oc] = f2key(xs[j]);
+          s.u.l.cpos[oc] = (uint32_t)(p0 + j);
+        }
+        ++oc;
+      }
+    }
+  }
+  return make_uint2(fa, fo);
+}
+
+// A multi-CTA row's boundary candidates of coarse digit b0 that did not fit the
+// staging list: written in chunk order to the row's candidate list from index base.
+__device__ __noinline__ void write_candidates_ordered(Ctx c, Unit u, int b0, int base) {
+  Smem& s = c.s;
+  const float4* b4 = reinterpret_cast<const float4*>(s.buf);
+  int cnt = 0;
+  for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
+    const float4 x = b4[v];
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) ++cnt;
+    }
+  }
+  int total;
+  int gi = base + block_excl_scan(cnt, &total, s);
+  for (int v = threadIdx.x; v < u.nvec && cnt > 0; v += kThreads) {
+    const float4 x = b4[v];
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * v - u.head + j;
+      if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) {
+        if (gi < kGroupCap) {
+          u.gs->cand_key[gi] = f2key(xs[j]);
+          u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
+        }
+        ++gi;
+      }
+    }
+  }
+}
+
+// A single-CTA row's boundary: `need` of its n staged candidates, emitted from `base`.
+__device__ __noinline__ void select_boundary_single(Ctx c, Unit u, int n, int need, int base) {
+  select_boundary(c, u, c.s.u.l.ckey, c.s.u.l.cpos, c.s.cst, n, need, base);
+}
+
+// A multi-CTA row with more than kRankOwnMax boundary candidates (gathered in lkey /
+// lpos, the same list in every CTA of the row): radix-select `need` of them (the same
+// marks in every CTA), then each CTA emits its own marked candidates, own0..own1, at
+// their position among the marked ones after the `above` values above the bin.
+__device__ __noinline__ void emit_listed(Ctx c, Unit u, const uint32_t* lkey,
+                                        const uint32_t* lpos, int n, int need, int own0,
+                                        int own1, int above) {
+  Smem& s = c.s;
+  list_select(s, lkey, lpos, s.cst, n, need);
+  int cnt = 0, before = 0;
+  for (int i = threadIdx.x; i < own0; i += kThreads)
+    if (s.cst[i] == kSel) ++before;
+  before = block_sum(before, s);
+  for (int i0 = own0; i0 < own1; i0 += kThreads) {
+    const int i = i0 + threadIdx.x;
+    const bool sel = i < own1 && s.cst[i] == kSel;
+    int total;
+    const int off = block_excl_scan(sel ? 1 : 0, &total, s);
+    if (sel) emit(c, u, above + before + cnt + off, (int)lpos[i]);
+    cnt += total;
+  }
+}
+
 // ------------------------------------------------------------- the unit
 
 __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
@@ -1001,7 +1167,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
 
   int b0, above0, eq0, la0, le0;
   u.blocal = 0;
-  if (!coarse_reduce(c, u, b0, above0, eq0, la0, le0)) return;
+  uint32_t pre = 0u;
+  bool pre_ok = false;
+  if (!coarse_reduce(c, u, b0, above0, eq0, la0, le0, pre, pre_ok)) return;
   TOPK_MARK(g_select_trace, 3);
 #ifdef TOPK_TRACE
   if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 28] = (uint64_t)s.bc[30] << 32;
@@ -1028,16 +1196,15 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   // thread revisits only its masked vectors. No shared atomics; the staging order is
   // deterministic. For a threshold bin on the positive side the bin's float bounds
   // are exact, so values are classified by compares alone and each vector's values go
-  // to their slots by popcounts of its compare masks, without branches.
+  // to their slots by popcounts of its compare masks, without branches. Other bins
+  // classify by digit, out of line (pass2_general).
   static_assert((kBufFloats / 4 + kThreads - 1) / kThreads <= 32,
                 "a thread's vectors of one chunk fit the 32-bit hit mask");
   const float tlo = skip_below((uint32_t)b0);
   const bool exact = b0 >= 2048 && b0 < 4095 && !fallback;
   const float thi = exact ? skip_below((uint32_t)b0 + 1u) : 0.0f;
   const float4* b4 = reinterpret_cast<const float4*>(s.buf);
-  uint32_t fa = 0xFFFFFFFFu, fo = 0u;
-  int na = 0, nc = 0;
-  uint32_t hm = 0u;  // bit i: this thread's i-th vector holds a value to stage
+  uint32_t fa = 0xFFFFFFFFu, fo = 0u;  // AND / OR of the boundary keys (fallback)
   // The chunk's first and last vectors may hold values of the neighbouring chunks:
   // those become -inf, below tlo (exact mode has tlo >= +0).
   const int vfull0 = (u.head + 3) >> 2, vfull1 = (u.head + u.n) >> 2;
@@ -1056,13 +1223,9 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     return (x.x >= t ? 1u : 0u) | (x.y >= t ? 2u : 0u) | (x.z >= t ? 4u : 0u) |
            (x.w >= t ? 8u : 0u);
   };
-  // classify one value (non-exact mode): 0 below, 1 above (staged position), 2 boundary
-  auto klass = [&](float x) -> int {
-    const uint32_t dg = coarse_digit(x);
-    if (dg < (uint32_t)b0) return 0;
-    return (dg > (uint32_t)b0 || all_eq) ? 1 : 2;
-  };
   if (exact) {
+    int na = 0, nc = 0;
+    uint32_t hm = 0u;  // bit i: this thread's i-th vector holds a value to stage
     auto count = [&](int i, int v, float4 x) {
       clip(v, x);
       const uint32_t mg = ge_mask(x, tlo);
@@ -1076,7 +1239,15 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     // one per 16 vectors, the usual case on long rows): most warps' vectors are all
     // below tlo, so a max filter skips them. Dense: every warp would take the branch,
     // so every vector is classified without one.
-    if ((int64_t)(la0 + le0) * 16 < u.nvec) {
+    if (pre_ok) {
+      // only the vectors marked while the first barrier propagated
+      for (uint32_t m = pre; m; m &= m - 1u) {
+        const int i = __ffs(m) - 1;
+        const int v = threadIdx.x + i * kThreads;
+        const float4 x = b4[v];
+        if (vmax4(x) >= tlo) count(i, v, x);
+      }
+    } else if ((int64_t)(la0 + le0) * 16 < u.nvec) {
       for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) {
         const float4 x = b4[v];
         if (vmax4(x) >= tlo) count(i, v, x);
@@ -1084,67 +1255,37 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
     } else {
       for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) count(i, v, b4[v]);
     }
-  } else {
-    for (int i = 0, v = threadIdx.x; v < u.nvec; ++i, v += kThreads) {
-      const float4 x = b4[v];
-      if (vmax4(x) < tlo) continue;
-      const int e0 = 4 * v - u.head;
-      const float xs[4] = {x.x, x.y, x.z, x.w};
-      int a = 0, cd = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = e0 + j;
-        if (e < 0 || e >= u.n) continue;
-        const int k = klass(xs[j]);
-        if (k == 1) {
-          ++a;
-        } else if (k == 2) {
-          ++cd;
-          if (fallback) {
-            const uint32_t key = f2key(xs[j]);
-            fa &= key;
-            fo |= key;
-          }
-        }
-      }
-      if (!stage_cand) cd = 0;
-      na += a;
-      nc += cd;
-      hm |= (a + cd) ? (1u << i) : 0u;
-    }
-  }
-  TOPK_LOG(u.r, 6);
+    TOPK_LOG(u.r, 6);
 #ifdef TOPK_TRACE_DETAIL  // block-wide timing; distorts the phases it brackets
-  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 18] = global_timer_ns();
-  {
-    // slowest thread of the count pass
-    __shared__ unsigned long long tmax;
-    if (threadIdx.x == 0) tmax = 0;
-    __syncthreads();
-    atomicMax(&tmax, (unsigned long long)global_timer_ns());
-    __syncthreads();
-    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 20] = tmax;
-    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 21] = __popc(hm);
-  }
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 18] = global_timer_ns();
+    {
+      // slowest thread of the count pass
+      __shared__ unsigned long long tmax;
+      if (threadIdx.x == 0) tmax = 0;
+      __syncthreads();
+      atomicMax(&tmax, (unsigned long long)global_timer_ns());
+      __syncthreads();
+      if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 20] = tmax;
+      if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 21] = __popc(hm);
+    }
 #endif
-  int tot_ac;
-  const int off_ac = block_excl_scan(na | (nc << 16), &tot_ac, s);
-  if (threadIdx.x == 0) {
-    s.bc[9] = tot_ac & 0xFFFF;  // staged emissions
-    s.bc[10] = tot_ac >> 16;    // staged candidates
-  }
-  TOPK_LOG(u.r, 7);
+    int tot_ac;
+    const int off_ac = block_excl_scan(na | (nc << 16), &tot_ac, s);
+    if (threadIdx.x == 0) {
+      s.bc[9] = tot_ac & 0xFFFF;  // staged emissions
+      s.bc[10] = tot_ac >> 16;    // staged candidates
+    }
+    TOPK_LOG(u.r, 7);
 #ifdef TOPK_TRACE
-  if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 19] = global_timer_ns();
+    if (threadIdx.x == 0) g_select_trace[blockIdx.x * 32 + 19] = global_timer_ns();
 #endif
-  int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
-  while (hm) {
-    const int i = __ffs(hm) - 1;
-    hm &= hm - 1u;
-    const int v = threadIdx.x + i * kThreads;
-    float4 x = b4[v];
-    const int p0 = u.s0 + 4 * v - u.head;  // position of component 0
-    if (exact) {
+    int oa = off_ac & 0xFFFF, oc = off_ac >> 16;
+    while (hm) {
+      const int i = __ffs(hm) - 1;
+      hm &= hm - 1u;
+      const int v = threadIdx.x + i * kThreads;
+      float4 x = b4[v];
+      const int p0 = u.s0 + 4 * v - u.head;  // position of component 0
       clip(v, x);
       const uint32_t mg = ge_mask(x, tlo);
       const uint32_t ma = all_eq ? mg : ge_mask(x, thi);
@@ -1163,25 +1304,11 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       }
       oa += __popc(ma);
       oc += __popc(mc);
-    } else {
-      const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = 4 * v - u.head + j;
-        if (e < 0 || e >= u.n) continue;
-        const int k = klass(xs[j]);
-        if (k == 1) {
-          if (oa < TOPK_MAX_K) s.u.l.elist[oa] = p0 + j;
-          ++oa;
-        } else if (k == 2 && stage_cand) {
-          if (oc < kListCap) {
-            s.u.l.ckey[oc] = f2key(xs[j]);
-            s.u.l.cpos[oc] = (uint32_t)(p0 + j);
-          }
-          ++oc;
-        }
-      }
     }
+  } else {
+    const uint2 f = pass2_general(c, u, b0, all_eq, fallback, stage_cand);
+    fa = f.x;
+    fo = f.y;
   }
 #ifdef TOPK_TRACE_DETAIL  // block-wide timing; distorts the phases it brackets
   {
@@ -1214,33 +1341,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
           u.gs->cand_pos[base + i] = s.u.l.cpos[i];
         }
     } else {
-      int cnt = 0;
-      for (int v = threadIdx.x; v < u.nvec; v += kThreads) {
-        const float4 x = b4[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) ++cnt;
-        }
-      }
-      int total;
-      int gi = base + block_excl_scan(cnt, &total, s);
-      for (int v = threadIdx.x; v < u.nvec && cnt > 0; v += kThreads) {
-        const float4 x = b4[v];
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * v - u.head + j;
-          if (e >= 0 && e < u.n && coarse_digit(xs[j]) == (uint32_t)b0) {
-            if (gi < kGroupCap) {
-              u.gs->cand_key[gi] = f2key(xs[j]);
-              u.gs->cand_pos[gi] = (uint32_t)(u.s0 + e);
-            }
-            ++gi;
-          }
-        }
-      }
+      write_candidates_ordered(c, u, b0, base);
     }
   };
   if (slots) write_candidates(u.rank * slot_cap);
@@ -1314,7 +1415,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   TOPK_LOG(u.r, 5);
   if (compact && u.G == 1) {
     __syncthreads();
-    select_boundary(c, u, s.u.l.ckey, s.u.l.cpos, s.cst, min(eq0, kListCap), need, above0);
+    select_boundary_single(c, u, min(eq0, kListCap), need, above0);
   }
 
   if (compact && u.G > 1) {
@@ -1405,21 +1506,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
       }
 #endif
     } else {
-      // radix-select among all candidates (same marks in every CTA), then each CTA
-      // emits its own marked candidates at their position among the marked ones
-      list_select(s, lkey, lpos, s.cst, n, need);
-      int cnt = 0, before = 0;
-      for (int i = threadIdx.x; i < own0; i += kThreads)
-        if (s.cst[i] == kSel) ++before;
-      before = block_sum(before, s);
-      for (int i0 = own0; i0 < own1; i0 += kThreads) {
-        const int i = i0 + threadIdx.x;
-        const bool sel = i < own1 && s.cst[i] == kSel;
-        int total;
-        const int off = block_excl_scan(sel ? 1 : 0, &total, s);
-        if (sel) emit(c, u, above0 + before + cnt + off, (int)lpos[i]);
-        cnt += total;
-      }
+      emit_listed(c, u, lkey, lpos, n, need, own0, own1, above0);
     }
     TOPK_MARK(g_select_trace, 7);
   }
@@ -1435,7 +1522,7 @@ __device__ void process_unit(Ctx& c, const UnitDesc& d, bool pre_issued) {
   TOPK_LOG(u.r, 8);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   const Layout lay = make_layout(p.rows);
@@ -1502,59 +1589,60 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(SelectParams p) {
   const bool pre_issued = s.bc[19] != 0;
   Ctx c{p, h, s, 0u};
   bool ran = false;  // a unit ran: s.bc[7] (aborting) is read after a CTA barrier
-  for (int w = 0; w < waves; ++w) {
-    UnitDesc d;
-    if (w == 0) {
-      d = s.ud;
-    } else {
-      __syncthreads();
-      if (ran && s.bc[7]) break;
-      if (threadIdx.x == 0) s.ud = units[(int64_t)w * kMaxGrid + blockIdx.x];
-      __syncthreads();
-      d = s.ud;
-    }
-    TOPK_LOG(d.row, 15);
-    if (d.row >= 0) {
-      process_unit(c, d, w == 0 && pre_issued);
-      ran = true;
-    }
-  }
-
+  // Units in one loop (one call site keeps the unit body inlined once): the static
+  // multi-CTA units of every wave, then the single row the plan hands this CTA (read
+  // in the prologue), then tickets. When the plan hands out every single row, no CTA
+  // claims one (each call then advances the ticket counter by 0, a multiple of its
+  // period, as the modular claims need).
   const int2* singles = reinterpret_cast<const int2*>(p.ws + lay.singles);
-  // The single row the plan hands this CTA (read in the prologue), then tickets; when
-  // the plan hands out every single row, no CTA claims one (each call then advances
-  // the ticket counter by 0, a multiple of its period, as the modular claims need).
   int idx = s.bc[29];
   bool implicit = idx >= 0;
   const bool tickets = n_single > n_implicit;
-  while (true) {
-    if (!implicit && !tickets) break;
-    if (ran) {
-      __syncthreads();
-      if (s.bc[7]) break;
-    }
-    if (!implicit) {
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const unsigned long long t = atomicAdd(&h->steal, 1ull);
-        s.bc[14] = n_implicit + (int)(t % (unsigned long long)dyn_period);
-      }
-      __syncthreads();
-      idx = s.bc[14];
-    }
-    implicit = false;
-    if (idx >= n_single) break;
-    const int2 sr = singles[idx];
+  for (int w = 0;;) {
     UnitDesc d;
-    d.row = sr.x;
-    d.s0 = 0;
-    d.len = sr.y;
-    d.n = (sr.y >= 0 && sr.y <= p.max_len) ? sr.y : 0;
-    d.rank = 0;
-    d.G = 1;
-    d.group = -1;
-    d.pad = 0;
-    process_unit(c, d, false);
+    bool pre = false;
+    if (w < waves) {
+      if (w == 0) {
+        d = s.ud;
+        pre = pre_issued;
+      } else {
+        __syncthreads();
+        if (ran && s.bc[7]) break;
+        if (threadIdx.x == 0) s.ud = units[(int64_t)w * kMaxGrid + blockIdx.x];
+        __syncthreads();
+        d = s.ud;
+      }
+      ++w;
+      TOPK_LOG(d.row, 15);
+      if (d.row < 0) continue;
+    } else {
+      if (!implicit && !tickets) break;
+      if (ran) {
+        __syncthreads();
+        if (s.bc[7]) break;
+      }
+      if (!implicit) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          const unsigned long long t = atomicAdd(&h->steal, 1ull);
+          s.bc[14] = n_implicit + (int)(t % (unsigned long long)dyn_period);
+        }
+        __syncthreads();
+        idx = s.bc[14];
+      }
+      implicit = false;
+      if (idx >= n_single) break;
+      const int2 sr = singles[idx];
+      d.row = sr.x;
+      d.s0 = 0;
+      d.len = sr.y;
+      d.n = (sr.y >= 0 && sr.y <= p.max_len) ? sr.y : 0;
+      d.rank = 0;
+      d.G = 1;
+      d.group = -1;
+      d.pad = 0;
+    }
+    process_unit(c, d, pre);
     ran = true;
   }
   if (ran) {

@@ -326,6 +326,37 @@ def test_cuda_graph_replay():
     compare_with_oracle(b, b.k, out.cpu().numpy(), pos.cpu().numpy())
 
 
+def test_chunks_that_open_with_their_largest_values():
+    """Long multi-CTA chunks count their first piece in full and then only values at or
+    above a pre-threshold taken from it. Here every CTA's chunk (1M rows over 21 CTAs)
+    opens with its largest values, so the pre-threshold leaves too few values counted
+    and each CTA completes its histogram from the resident chunk; a second batch holds
+    the row's whole top in its first chunk, which also sends the row through the round
+    that publishes every bin."""
+    rng = np.random.default_rng(23)
+    L, G = 1_000_000, 21
+    c = -(-(-(-L // G)) // 16) * 16  # each CTA's chunk of a 21-CTA row
+    ramp = (6.0 - 12.0 * (np.arange(L + 6) % c) / c).astype(np.float32)
+    lens = np.arange(L, L + 7, dtype=np.int32)
+    s = np.full((7, W.round_up(L + 6, 4)), W.POISON, np.float32)
+    for r in range(7):
+        s[r, :lens[r]] = ramp[:lens[r]] + 0.05 * rng.standard_normal(lens[r]).astype(np.float32)
+    tab = rng.permutation(-(-(L + 6) // 64)).astype(np.int32).reshape(1, -1)
+    b = W.Batch("chunk_ramps", s, lens, L + 6, 2048, tab, np.zeros(7, np.int32), 64)
+    for k in (1, 100, 2048):
+        slots, pos, st = run_gpu(b, k=k)
+        assert st == 0, B.status_str(st)
+        compare_with_oracle(b, k, slots, pos)
+    top = s.copy()
+    for r in range(7):
+        top[r, :lens[r]] = np.sort(s[r, :lens[r]])[::-1]
+    bt = dataclasses.replace(b, name="row_top_first", scores=top)
+    for k in (100, 2048):
+        slots, pos, st = run_gpu(bt, k=k)
+        assert st == 0, B.status_str(st)
+        compare_with_oracle(bt, k, slots, pos)
+
+
 def test_skewed_rows_over_many_ctas():
     """Rows whose top values are not spread evenly over the CTAs that share them:
     sorted descending (one chunk holds the whole top-k, so the bins each CTA publishes
