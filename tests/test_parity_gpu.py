@@ -327,12 +327,11 @@ def test_cuda_graph_replay():
 
 
 def test_chunks_that_open_with_their_largest_values():
-    """Long multi-CTA chunks count their first piece in full and then only values at or
-    above a pre-threshold taken from it. Here every CTA's chunk (1M rows over 21 CTAs)
-    opens with its largest values, so the pre-threshold leaves too few values counted
-    and each CTA completes its histogram from the resident chunk; a second batch holds
-    the row's whole top in its first chunk, which also sends the row through the round
-    that publishes every bin."""
+    """Chunk-local skew at the 1M verify shape (21 CTAs per row): every CTA's chunk
+    opens with its largest values, so each CTA's own threshold bin, and the vectors it
+    marks at that bin while the first barrier propagates, come from the chunk's first
+    pieces. A second batch holds each row's whole top in its first chunk, so the bins
+    the CTAs publish first cannot fix the threshold and the row publishes the rest."""
     rng = np.random.default_rng(23)
     L, G = 1_000_000, 21
     c = -(-(-(-L // G)) // 16) * 16  # each CTA's chunk of a 21-CTA row
