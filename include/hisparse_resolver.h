@@ -65,8 +65,9 @@ enum {
   RESOLVER_STATUS_KV_ROW = 8     /* a victim's KV row outside [0, kv_rows) */
 };
 
-/* One launch on `stream` (one CTA per request); argument errors return before
- * anything is enqueued.
+/* One launch on `stream`: one CTA per request owns its state; when the batch leaves
+ * SMs free, each request is a cluster of 2, 4 or 8 CTAs that share its row copies.
+ * Argument errors return before anything is enqueued.
  *   positions    device int32 [rows, k]: selected positions, -1 padding
  *   block_table  device int32 [rows, table_ld]: block id, or < 0 (host only)
  *   token_to_hot device int32 [rows, map_ld]: slot holding each position, -1 none
@@ -90,7 +91,7 @@ int hisparse_resolve(const int32_t* positions, int rows, int k, const int32_t* b
 
 /* The same for q_rows query rows per request (q_rows >= 1): positions and out_rows
  * are [rows, q_rows, k]; request j's rows are resolved in order q = 0 .. q_rows - 1 at
- * step `step`, by the request's one CTA; counts sum over its rows. Other arguments,
+ * step `step`, by the CTA that owns the request; counts sum over its rows. Other arguments,
  * return codes and status bits as hisparse_resolve (RESOLVER_ERR_SHAPE also for
  * q_rows < 1). */
 int hisparse_resolve_mtp(const int32_t* positions, int rows, int q_rows, int k,

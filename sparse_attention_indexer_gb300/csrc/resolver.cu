@@ -11,6 +11,13 @@
 // (read directly by the kernel, eight 16-byte chunks per thread in flight) into the
 // victims' KV rows. Every phase issues its independent loads together: one CTA per
 // request leaves little other parallelism to hide their latency.
+//
+// The host reads of one SM do not go faster with more of them in flight, so a batch of
+// few requests runs each request as a thread-block cluster: CTA 0 of the cluster owns
+// the request's state and does everything above; once its copy list is complete (a
+// cluster barrier), every CTA of the cluster copies a share of the rows, reading the
+// list from CTA 0's shared memory, and a second cluster barrier ends the row's copies
+// before the list is reused.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -48,6 +55,7 @@ struct Params {
   int32_t* counts;
   int32_t* status;
   int q_rows;  // query rows per request, resolved one after another at the same step
+  int csize;   // CTAs per request (a cluster when > 1); CTA 0 owns the request
 };
 
 struct Smem {
@@ -60,12 +68,79 @@ struct Smem {
   uint8_t hit_slot[kMaxHot];  // slots refreshed by a hit of this step
   int64_t copy_src[kMaxK];    // host row of each assigned miss (by rank), -1 none
   int32_t copy_dst[kMaxK];    // KV row
+  int32_t n_list;             // entries of copy_src / copy_dst for this query row
   int32_t wsum[kThreads / 32];
   uint64_t wsum2[2][kThreads / 32];
   int32_t red[4][kThreads / 32];
 };
 
 static_assert(offsetof(Smem, hit_slot) % 8 == 0, "hit bitmap zeroed with 8-byte stores");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster: shared-memory writes before it are seen by
+// the cluster's shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Address in the cluster's shared window of `p` (this CTA's shared memory) in CTA 0.
+__device__ __forceinline__ uint32_t in_rank0(const void* p) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(p), r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ int64_t ld_cluster_s64(uint32_t a) {
+  int64_t v;
+  asm volatile("ld.shared::cluster.s64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int32_t ld_cluster_s32(uint32_t a) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// The row copies of one query row, shared among the request's csize CTAs (crank = this
+// CTA's rank): (miss, 16-byte chunk) pairs, eight per thread in flight, loads first and
+// then the stores. The list (n entries) is CTA 0's; other CTAs read it through the
+// cluster's shared window.
+__device__ __noinline__ void copy_rows(const Params& p, Smem& s, int crank, int n) {
+  const int chunks = p.row_bytes >> 4;
+  const int64_t total = (int64_t)n * chunks;
+  const int64_t stride = (int64_t)p.csize * kThreads;
+  const uint32_t src0 = crank > 0 ? in_rank0(&s.copy_src[0]) : 0u;
+  const uint32_t dst0 = crank > 0 ? in_rank0(&s.copy_dst[0]) : 0u;
+  constexpr int kC = 8;
+  for (int64_t c0 = (int64_t)crank * kThreads + threadIdx.x; c0 < total; c0 += kC * stride) {
+    uint4 v[kC];
+    int64_t dst[kC];
+#pragma unroll
+    for (int e = 0; e < kC; ++e) {
+      const int64_t c = c0 + e * stride;
+      dst[e] = -1;
+      if (c < total) {
+        const int rr = (int)(c / chunks), cq = (int)(c - (int64_t)rr * chunks);
+        const int64_t src = crank > 0 ? ld_cluster_s64(src0 + 8u * rr) : s.copy_src[rr];
+        if (src >= 0) {
+          const int32_t kr = crank > 0 ? ld_cluster_s32(dst0 + 4u * rr) : s.copy_dst[rr];
+          v[e] = *reinterpret_cast<const uint4*>(p.host + src * p.row_bytes + 16 * cq);
+          dst[e] = (int64_t)kr * p.row_bytes + 16 * cq;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kC; ++e)
+      if (dst[e] >= 0) *reinterpret_cast<uint4*>(p.kv + dst[e]) = v[e];
+  }
+}
 
 __device__ int block_excl_scan(int v, int* total, Smem& s) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -91,10 +166,22 @@ __device__ int block_excl_scan(int v, int* total, Smem& s) {
 // kRows: the request has several query rows (a loop over them); else exactly one, and
 // the body compiles without the loop (the loop costs the one-row step registers).
 template <bool kRows>
-__global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads) resolve_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
-  const int j = blockIdx.x;
+  const int j = blockIdx.x / p.csize;
+  const int n_rows = kRows ? p.q_rows : 1;
+  if (p.csize > 1 && cluster_rank() != 0) {
+    // A copying CTA of the request: its share of each query row's copies.
+    const int crank = (int)cluster_rank();
+    const uint32_t nl = in_rank0(&s.n_list);
+    for (int qr = 0; qr < n_rows; ++qr) {
+      cluster_sync();  // CTA 0's list for this row is complete
+      copy_rows(p, s, crank, ld_cluster_s32(nl));
+      cluster_sync();  // every CTA is done with the list
+    }
+    return;
+  }
   const int32_t* tab = p.table + (int64_t)j * p.table_ld;
   int32_t* t2h = p.t2h + (int64_t)j * p.map_ld;
   int32_t* htok = p.hot_token + (int64_t)j * p.hot;
@@ -104,7 +191,6 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
   // The request's query rows, one after another: a later row sees the state an earlier
   // one left (its misses are hits now, and the slots it used, at this step, are not
   // victims). Global writes of the block are visible to it after each row's barrier.
-  const int n_rows = kRows ? p.q_rows : 1;
   for (int qr = 0; qr < n_rows; ++qr) {
   const int32_t* pos = p.positions + ((int64_t)j * p.q_rows + qr) * p.k;
   int32_t* out = p.out + ((int64_t)j * p.q_rows + qr) * p.k;
@@ -488,33 +574,17 @@ __global__ void __launch_bounds__(kThreads) resolve_kernel(Params p) {
     }
     __syncthreads();
 
-    // 5. copies: (miss, 16-byte chunk) pairs spread over the block
-    // eight chunks per thread in flight: loads first, then the stores (more in flight per
-    // thread measured slower: the host reads of one SM do not go faster)
-    const int chunks = p.row_bytes >> 4;
-    const int64_t total = (int64_t)m * chunks;
-    constexpr int kC = 8;
-    for (int64_t c0 = threadIdx.x; c0 < total; c0 += (int64_t)kC * kThreads) {
-      uint4 v[kC];
-      int64_t dst[kC];
-#pragma unroll
-      for (int e = 0; e < kC; ++e) {
-        const int64_t c = c0 + (int64_t)e * kThreads;
-        dst[e] = -1;
-        if (c < total) {
-          const int rr = (int)(c / chunks), cq = (int)(c - (int64_t)rr * chunks);
-          const int64_t src = s.copy_src[rr];
-          if (src >= 0) {
-            v[e] = *reinterpret_cast<const uint4*>(p.host + src * p.row_bytes + 16 * cq);
-            dst[e] = (int64_t)s.copy_dst[rr] * p.row_bytes + 16 * cq;
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < kC; ++e)
-        if (dst[e] >= 0) *reinterpret_cast<uint4*>(p.kv + dst[e]) = v[e];
-    }
     for (int rr = threadIdx.x; rr < m; rr += kThreads) n_copy += s.copy_src[rr] >= 0 ? 1 : 0;
+  }
+  // 5. copies of this row's misses, over the request's CTAs
+  if (threadIdx.x == 0) s.n_list = m;
+  if (p.csize > 1) {
+    cluster_sync();
+    copy_rows(p, s, 0, m);
+    cluster_sync();
+  } else {
+    __syncthreads();
+    copy_rows(p, s, 0, m);
   }
   __syncthreads();  // this row's state writes are seen by the next row
   }  // query rows
@@ -585,14 +655,37 @@ int resolve_launch(const int32_t* positions, int rows, int q_rows, int k, const 
       return RESOLVER_ERR_CUDA;
     attr_set = true;
   }
+  // CTAs per request: the largest cluster size (8, 4, 2) that keeps every request's
+  // cluster resident at once (one CTA per SM), else 1.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RESOLVER_ERR_CUDA;
+  int csize = 8;
+  while (csize > 1 && (int64_t)rows * csize > sms) csize >>= 1;
   Params p{positions, rows,     k,        block_table, table_ld,  page_size, token_to_hot,
            map_ld,    hot_token, hot_step, hot_rows,    hot_size,  step,      host_kv,
            host_base, host_rows, kv,       kv_rows,     row_bytes, out_rows,  counts,
-           status,    q_rows};
-  if (q_rows == 1)
-    resolve_kernel<false><<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
-  else
-    resolve_kernel<true><<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
+           status,    q_rows,    csize};
+  void (*fn)(Params) = q_rows == 1 ? resolve_kernel<false> : resolve_kernel<true>;
+  if (csize > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(rows * csize));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    cfg.stream = (cudaStream_t)stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fn, p) == cudaSuccess) return RESOLVER_OK;
+    (void)cudaGetLastError();  // clusters refused: one CTA per request
+    p.csize = 1;
+  }
+  fn<<<rows, kThreads, sizeof(Smem), (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? RESOLVER_OK : RESOLVER_ERR_CUDA;
 }
 
