@@ -233,3 +233,28 @@ def test_mtp_single_row_equals_the_plain_call():
                    n_steps=3)
     import dataclasses
     run_mtp_sequence(dataclasses.replace(b, steps=[s[:, None, :] for s in b.steps]))
+
+
+@pytest.mark.parametrize("reqs", [20, 40, 160])
+def test_batches_of_every_cluster_size(reqs):
+    """The requests of a batch that leaves SMs free run as clusters that share their row
+    copies (8, 4 or 2 CTAs per request by the batch size and the SM count); a batch of
+    more requests than SMs runs one CTA per request. 20, 40 and 160 requests take
+    clusters of 4, 2 and none on a 152-SM GPU (the size is the library's choice: the
+    result must not depend on it)."""
+    rng = np.random.default_rng(reqs)
+    lens = rng.integers(800, 6000, reqs).tolist()
+    b = W.hisparse(seed=W.SEED_BASE + 80 + reqs, reqs=reqs, k=64, lens=lens, tail=256,
+                   row_bytes=48, n_steps=3)
+    total = run_sequence(b)
+    assert total[:, 2].sum() > 0
+
+
+def test_mtp_batch_of_clusters_of_four():
+    """A multi-token batch of 20 requests: each query row's copies are shared by the
+    request's cluster, and the cluster meets twice per row."""
+    b = W.hisparse_mtp(seed=W.SEED_BASE + 79, reqs=20, k=64, q_rows=4,
+                       lens=np.random.default_rng(5).integers(800, 5000, 20).tolist(),
+                       tail=256, row_bytes=32, n_steps=3)
+    total = run_mtp_sequence(b)
+    assert total[:, 2].sum() > 0
