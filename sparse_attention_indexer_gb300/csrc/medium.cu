@@ -70,6 +70,11 @@ static_assert(kMediumMaxLen <= 64 * kMedThreads, "a thread's entries of a row fi
 // `identity`), written with the positions; eight table reads per thread in flight.
 __device__ __forceinline__ void med_translate(const SelectParams& P, MedShared& S, int32_t* os,
                                               int32_t* op, int t, int kr, bool identity) {
+  // a page size that is a power of two divides by a shift (the usual case, 64)
+  const int ps = P.page_size;
+  const bool pow2 = (ps & (ps - 1)) == 0;
+  const int sh = __ffs(ps) - 1;
+  const int32_t* trow = P.table + (int64_t)t * P.table_ld;
   for (int o0 = 0; o0 < kr; o0 += 8 * kMedThreads) {
     int pp[8];
     int32_t pg[8];
@@ -77,13 +82,14 @@ __device__ __forceinline__ void med_translate(const SelectParams& P, MedShared& 
     for (int j = 0; j < 8; ++j) {
       const int o = o0 + j * kMedThreads + (int)threadIdx.x;
       pp[j] = o < kr ? (identity ? o : (int)S.outp[o]) : -1;
-      pg[j] = pp[j] >= 0 ? __ldg(P.table + (int64_t)t * P.table_ld + pp[j] / P.page_size) : 0;
+      pg[j] = pp[j] >= 0 ? __ldg(trow + (pow2 ? pp[j] >> sh : pp[j] / ps)) : 0;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int o = o0 + j * kMedThreads + (int)threadIdx.x;
       if (pp[j] < 0) continue;
-      const int64_t sl = (int64_t)pg[j] * P.page_size + pp[j] % P.page_size;
+      const int in = pow2 ? pp[j] & (ps - 1) : pp[j] % ps;
+      const int64_t sl = (int64_t)pg[j] * ps + in;
       int32_t v = (int32_t)sl;
       if (pg[j] < 0) {
         atomicOr(&S.status, TOPK_STATUS_TABLE_ENTRY);
@@ -113,11 +119,13 @@ __device__ __forceinline__ int med_bins(int lv) { return lv == 0 ? kCoarseBins :
 // above d) < need <= (values at or above d). Thread t scans bins [t * per, ...) from
 // the top; the block adds up the ranges above each thread.
 __device__ void med_boundary(MedShared& S, int nb, int need) {
+  // nb is 4096, 256 or 128: a thread's range is 16 bins or 1 (or empty past nb)
   const int per = (nb + kMedThreads - 1) / kMedThreads;
   const int lo = min(nb, (int)threadIdx.x * per), hi = min(nb, lo + per);
   int mine = 0;
   // lanes read their ranges in rotated order, so one load touches distinct banks
-  for (int i = 0; i < hi - lo; ++i) mine += S.hist[lo + ((i + (int)threadIdx.x) % (hi - lo))];
+  if (hi - lo == per)
+    for (int i = 0; i < per; ++i) mine += S.hist[lo + ((i + (int)threadIdx.x) & (per - 1))];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = mine;  // sum over lanes [lane, 31] of this warp
 #pragma unroll
@@ -412,27 +420,33 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       if (fast) {
         // coarse level, boundary on the positive side: four values per step, bit
         // 4 step + c of the masks for position 4 (step * threads + t) + c
+        // 4-bit compare masks per vector: above the bin, at or above it (NaN compares
+        // false; a NaN bound keeps the top bin's "above" empty, +inf included)
         const int nv = (L + 3) >> 2;
+        const float ta = d < 4095u ? t_above : __int_as_float(0x7FC00000);
         int jb = 0;
         for (int v0 = 0; v0 < nv; v0 += kMedThreads, jb += 4) {
           const int v = v0 + (int)threadIdx.x;
           if (v >= nv) continue;
           const float4 q = reinterpret_cast<const float4*>(sx)[v];
-          const float e[4] = {q.x, q.y, q.z, q.w};
+          const uint32_t vm = 4 * v + 4 <= L ? 0xFu : (1u << (L - 4 * v)) - 1u;  // the row's tail
+          const uint32_t a_n = ((q.x >= ta ? 1u : 0u) | (q.y >= ta ? 2u : 0u) |
+                                (q.z >= ta ? 4u : 0u) | (q.w >= ta ? 8u : 0u)) & vm;
+          const uint32_t g_n = ((q.x >= t_at ? 1u : 0u) | (q.y >= t_at ? 2u : 0u) |
+                                (q.z >= t_at ? 4u : 0u) | (q.w >= t_at ? 8u : 0u)) & vm;
+          const uint32_t at_n = g_n & ~a_n;
+          if (at_n) {
+            const float e[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float x = 4 * v + c < L ? e[c] : __int_as_float(0xFF800000);  // -inf: below every bin >= 2048
-            const bool above_bin = d < 4095u && x >= t_above;
-            const bool at_bin = !above_bin && x >= t_at;
-            const int cls = above_bin || (ends && at_bin) ? 1 : (list && at_bin ? 2 : 0);
-            if (at_bin) {
-              const uint32_t key = f2key(x);
-              kand &= key;
-              kor |= key;
-            }
-            m_take |= (uint64_t)(cls == 1) << (jb + c);
-            m_keep |= (uint64_t)(cls == 2) << (jb + c);
+            for (int c = 0; c < 4; ++c)
+              if ((at_n >> c) & 1u) {
+                const uint32_t key = f2key(e[c]);
+                kand &= key;
+                kor |= key;
+              }
           }
+          m_take |= (uint64_t)(a_n | (ends ? at_n : 0u)) << jb;
+          m_keep |= (uint64_t)(list ? at_n : 0u) << jb;
         }
       } else {
         int j = 0;
