@@ -28,16 +28,23 @@ SENTINEL_CODE = 0xAA
 SENTINEL_SCALE = -7.0
 
 
-def run_both(b: W.KeyBatch):
-    """(gpu cache, gpu scales, gpu status), (oracle cache, scales, status, y, slots)."""
+def run_both(b: W.KeyBatch, cs_offset: int = 0):
+    """(gpu cache, gpu scales, gpu status), (oracle cache, scales, status, y, slots).
+    cs_offset > 0 places the cos/sin table that many floats into a larger buffer (an
+    address without 16-byte alignment)."""
     dev = torch.device("cuda", 0)
+    cs = torch.from_numpy(b.cos_sin).to(dev)
+    if cs_offset:
+        buf = torch.zeros(cs.numel() + cs_offset, dtype=torch.float32, device=dev)
+        buf[cs_offset:] = cs.reshape(-1)
+        cs = buf[cs_offset:].view(cs.shape)
     cache = torch.full((b.num_slots, b.dim), SENTINEL_CODE, dtype=torch.uint8, device=dev)
     scales = torch.full((b.num_slots,), SENTINEL_SCALE, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.indexer_k_prologue(torch.from_numpy(b.k_bf16.view(np.int16)).to(dev),
                          torch.from_numpy(b.ln_w).to(dev), torch.from_numpy(b.ln_b).to(dev),
                          b.eps, torch.from_numpy(b.positions).to(dev),
-                         torch.from_numpy(b.cos_sin).to(dev), b.rope_dim,
+                         cs, b.rope_dim,
                          torch.from_numpy(b.token_table).to(dev),
                          torch.from_numpy(b.block_table).to(dev), b.page_size, cache, scales,
                          status=status)
@@ -89,11 +96,22 @@ def test_workload_multi_request():
     compare(*run_both(b))
 
 
-@pytest.mark.parametrize("rope_dim", [0, 2, 6, 64, 128])
+@pytest.mark.parametrize("rope_dim", [0, 2, 6, 24, 64, 128])
 def test_rope_widths(rope_dim):
+    """Rotated widths from none to all 128 channels; a lane holds channels 8h .. 8h + 7,
+    so at 2 and 6 one lane rotates part of its pairs and at 24 three lanes rotate all of
+    theirs while the rest rotate none."""
     b = W.key_prologue(seed=W.SEED_BASE + 60 + rope_dim, reqs=((0, 700), (5000, 300)),
                        rope_dim=rope_dim, max_pos=8192)
     compare(*run_both(b))
+
+
+def test_unaligned_rope_table():
+    """A cos/sin table at an address without 16-byte alignment (the header asks for
+    4-byte alignment only)."""
+    b = W.key_prologue(seed=W.SEED_BASE + 69, reqs=((0, 700), (5000, 300)), rope_dim=64,
+                       max_pos=8192)
+    compare(*run_both(b, cs_offset=1))
 
 
 def test_page_sizes_and_tables():
