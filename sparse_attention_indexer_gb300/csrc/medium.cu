@@ -152,20 +152,22 @@ __device__ void med_boundary(MedShared& S, int nb, int need) {
   __syncthreads();
 }
 
-// One warp selects the `need` best of the n listed positions (n <= 32 * kFinishPer):
+// One warp selects the `need` best of the n listed positions (n <= 32 * kPer):
 // lane l holds positions list[l + 32 c] as 64-bit composite keys (score key << 14 |
 // 16383 - position, all distinct), and a radix selection runs from the highest bit
 // where they differ, one warp-wide count per bit. The selected positions are appended
-// to S.outp after the S.emitted already there.
+// to S.outp after the S.emitted already there. kPer (values per lane) is the smallest
+// that holds n, so each bit's step touches no more registers than needed.
+template <int kPer>
 __device__ void med_warp_finish(MedShared& S, const float* sx, const uint16_t* list, int n, int need,
                                 int kr) {
   const int lane = threadIdx.x & 31;
-  uint64_t key[kFinishPer];
-  int pos[kFinishPer];
+  uint64_t key[kPer];
+  int pos[kPer];
   uint32_t cand = 0u;
   uint32_t an_hi = 0xFFFFFFFFu, an_lo = 0xFFFFFFFFu, or_hi = 0u, or_lo = 0u;
 #pragma unroll
-  for (int c = 0; c < kFinishPer; ++c) {
+  for (int c = 0; c < kPer; ++c) {
     const int i = lane + 32 * c;
     key[c] = 0ull;
     pos[c] = 0;
@@ -191,7 +193,7 @@ __device__ void med_warp_finish(MedShared& S, const float* sx, const uint16_t* l
     for (int bit = 63 - __clzll((long long)diff); bit >= 0 && need > 0; --bit) {
       uint32_t m1 = 0u;
 #pragma unroll
-      for (int c = 0; c < kFinishPer; ++c) m1 |= (uint32_t)((key[c] >> bit) & 1ull) << c;
+      for (int c = 0; c < kPer; ++c) m1 |= (uint32_t)((key[c] >> bit) & 1ull) << c;
       m1 &= cand;
       const int cnt = (int)__reduce_add_sync(0xffffffffu, (unsigned)__popc(m1));
       if (cnt >= need) {
@@ -211,7 +213,7 @@ __device__ void med_warp_finish(MedShared& S, const float* sx, const uint16_t* l
   const unsigned lt = (1u << lane) - 1u;
   int base = S.emitted;
 #pragma unroll
-  for (int c = 0; c < kFinishPer; ++c) {
+  for (int c = 0; c < kPer; ++c) {
     const bool s = (sel >> c) & 1u;
     const unsigned b = __ballot_sync(0xffffffffu, s);
     if (s) {
@@ -370,7 +372,13 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
     for (int lv = 0; lv < kLevels && need > 0; ++lv) {
       if (src >= 0 && n_src <= 32 * kFinishPer) {
         // few values left, listed: one warp selects `need` of them in registers
-        if (threadIdx.x < 32) med_warp_finish(S, sx, med_list(S, src), n_src, need, kr);
+        if (threadIdx.x < 32) {
+          const uint16_t* l = med_list(S, src);
+          if (n_src <= 32) med_warp_finish<1>(S, sx, l, n_src, need, kr);
+          else if (n_src <= 64) med_warp_finish<2>(S, sx, l, n_src, need, kr);
+          else if (n_src <= 128) med_warp_finish<4>(S, sx, l, n_src, need, kr);
+          else med_warp_finish<8>(S, sx, l, n_src, need, kr);
+        }
         __syncthreads();
         need = 0;
         break;
