@@ -424,6 +424,7 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       const bool fast = lv == 0 && d >= 2048u;
       const float t_at = skip_below(d), t_above = d < 4095u ? skip_below(d + 1u) : 0.0f;
       uint64_t m_take = 0ull, m_keep = 0ull;
+      uint32_t t_lo = 0u, t_hi = 0u, k_lo = 0u, k_hi = 0u;  // their 32-bit halves (coarse level)
       uint32_t kand = 0xFFFFFFFFu, kor = 0u;  // keys of the coarse boundary bin's values
       if (fast) {
         // coarse level, boundary on the positive side: four values per step, bit
@@ -453,9 +454,17 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
                 kor |= key;
               }
           }
-          m_take |= (uint64_t)(a_n | (ends ? at_n : 0u)) << jb;
-          m_keep |= (uint64_t)(list ? at_n : 0u) << jb;
+          const uint32_t tn = a_n | (ends ? at_n : 0u), kn = list ? at_n : 0u;
+          if (jb < 32) {  // the same for the whole warp
+            t_lo |= tn << jb;
+            k_lo |= kn << jb;
+          } else {
+            t_hi |= tn << (jb - 32);
+            k_hi |= kn << (jb - 32);
+          }
         }
+        m_take = (uint64_t)t_hi << 32 | t_lo;
+        m_keep = (uint64_t)k_hi << 32 | k_lo;
       } else {
         int j = 0;
         for (int i0 = 0; i0 < n_src; i0 += kMedThreads, ++j) {
@@ -485,16 +494,35 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       }
       int o = __shfl_sync(0xffffffffu, o_base, 31) + s_take - c_take;
       int c = __shfl_sync(0xffffffffu, c_base, 31) + s_keep - c_keep;
-      for (uint64_t m = m_take | m_keep; m; m &= m - 1) {
-        const int js = __ffsll((long long)m) - 1;
-        const int i = js * kMedThreads + (int)threadIdx.x;
-        const int p = fast ? 4 * ((js >> 2) * kMedThreads + (int)threadIdx.x) + (js & 3)
-                           : src >= 0 ? (int)med_list(S, src)[i] : i;
-        if ((m_take >> js) & 1ull) {
+      if (fast) {
+        // bit js of a mask is component js & 3 of the thread's vector js >> 2; each
+        // mask half is walked on its own (32-bit steps, no test of which mask)
+        const int p0 = 4 * (int)threadIdx.x;
+        auto pos_of = [&](int js) { return p0 + 4 * kMedThreads * (js >> 2) + (js & 3); };
+        for (uint32_t m = t_lo; m; m &= m - 1u) {
+          const int p = pos_of(__ffs(m) - 1);
           if (o < kr) S.outp[o] = (uint16_t)p;  // o < kr by construction; guarded
           ++o;
-        } else {
-          med_list(S, dst)[c++] = (uint16_t)p;
+        }
+        for (uint32_t m = t_hi; m; m &= m - 1u) {
+          const int p = pos_of(__ffs(m) + 31);
+          if (o < kr) S.outp[o] = (uint16_t)p;
+          ++o;
+        }
+        uint16_t* dl = med_list(S, dst);
+        for (uint32_t m = k_lo; m; m &= m - 1u) dl[c++] = (uint16_t)pos_of(__ffs(m) - 1);
+        for (uint32_t m = k_hi; m; m &= m - 1u) dl[c++] = (uint16_t)pos_of(__ffs(m) + 31);
+      } else {
+        for (uint64_t m = m_take | m_keep; m; m &= m - 1) {
+          const int js = __ffsll((long long)m) - 1;
+          const int i = js * kMedThreads + (int)threadIdx.x;
+          const int p = src >= 0 ? (int)med_list(S, src)[i] : i;
+          if ((m_take >> js) & 1ull) {
+            if (o < kr) S.outp[o] = (uint16_t)p;  // o < kr by construction; guarded
+            ++o;
+          } else {
+            med_list(S, dst)[c++] = (uint16_t)p;
+          }
         }
       }
       if (fast) {
