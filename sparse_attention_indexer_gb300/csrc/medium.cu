@@ -225,13 +225,12 @@ __device__ void med_warp_finish(MedShared& S, const float* sx, const uint16_t* l
   if (lane == 0) S.emitted = base;
 }
 
-// Bulk prefetch of row r's scores into L2 (whole 16-byte units from an aligned start;
-// an unaligned row is not prefetched).
+// Bulk prefetch of row r's scores into L2: its first max_len values (inside the score
+// array, whose rows are ld >= max_len apart), so that the row's length need not be read
+// first; whole 16-byte units from an aligned start, an unaligned row not at all.
 __device__ __forceinline__ void med_prefetch_row(const SelectParams& P, int r) {
-  const int L = __ldg(P.lens + r);
-  if (L <= P.k || L > P.max_len) return;
   const float* row = P.scores + (int64_t)r * P.ld;
-  const uint32_t bytes = (uint32_t)(L * 4) & ~15u;
+  const uint32_t bytes = (uint32_t)(P.max_len * 4) & ~15u;
   if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0 || bytes == 0) return;
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"(bytes) : "memory");
 }
