@@ -277,11 +277,18 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
   // round trip stays off the row's path.
   const unsigned long long period = (unsigned long long)P.rows + gridDim.x;
   unsigned long long pending = 0ull;  // thread 0: the claimed next ticket
+  int nx = -1;                        // thread 0: its row, once computed
+  // ticket -> row; a 32-bit remainder while the ticket counter fits (the 64-bit one is
+  // a long software sequence on thread 0's path, which the CTA waits for)
+  auto row_of = [&](unsigned long long tk) {
+    return tk <= 0xFFFFFFFFull ? (int)((uint32_t)tk % (uint32_t)period) : (int)(tk % period);
+  };
   if (threadIdx.x == 0) pending = atomicAdd(&h->med_ticket, 1ull);
   while (true) {
     __syncthreads();
     if (threadIdx.x == 0) {
-      row_sh = (int)(pending % period);
+      row_sh = nx >= 0 ? nx : row_of(pending);
+      nx = -1;
       if (row_sh < P.rows) pending = atomicAdd(&h->med_ticket, 1ull);
       S.emitted = 0;
       S.status = 0;
@@ -315,7 +322,8 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
     }
 
     // Load the row into shared memory; histogram the coarse digit; AND / OR the keys.
-    for (int i = threadIdx.x; i < kCoarseBins; i += kMedThreads) S.hist[i] = 0;
+    for (int i = threadIdx.x; i < kCoarseBins / 4; i += kMedThreads)
+      reinterpret_cast<int4*>(S.hist)[i] = make_int4(0, 0, 0, 0);
     __syncthreads();
     const float* row = P.scores + (int64_t)r * P.ld;
     int head = 0;  // scalar positions start here
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       }
       med_boundary(S, nb, need);
       if (lv == 0 && threadIdx.x == 0) {
-        const int nx = (int)(pending % period);
+        nx = row_of(pending);
         if (nx < P.rows) med_prefetch_row(P, nx);
       }
       const uint32_t d = (uint32_t)S.bnd_digit;
