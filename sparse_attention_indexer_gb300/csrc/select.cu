@@ -16,8 +16,13 @@
 //
 // Multi-CTA rows publish the histogram bins at or above each CTA's own local
 // threshold bin (the row's threshold cannot lie lower) and meet at a bounded spin
-// barrier (co-residency is guaranteed by the cooperative launch). The row's last CTA
-// to finish ranks the boundary candidates exactly and clears the row's counters.
+// barrier (co-residency is guaranteed by the cooperative launch); while it propagates
+// each CTA marks the vectors that reach its own bin. A second barrier delivers every
+// CTA's counts and boundary candidates: each CTA then writes its staged positions at
+// its row offset, ranks its own candidates against all of the row's, and clears the
+// histogram bins it published. Rarely taken paths (general pass 2, large boundary
+// sets, massive ties) are out-of-line functions, so that the common path's code stays
+// compact when it is fetched cold.
 #include <cuda_runtime.h>
 
 #include <cstdint>
