@@ -815,7 +815,7 @@ def run_ours(args):
             "rows_resolved_per_s": round(rb.rows * 2048 / (rv_ms / 1e3), 1),
             "host_bytes_copied": rv_copy,
             "host_read_gbs": round(rv_copy / (rv_ms / 1e3) / 1e9, 2),
-            "bound": "latency (one CTA per request: classify, LRU sort, host round trip)",
+            "bound": "latency (one CTA per request owns its state: classify, LRU order, remap; a cluster of up to 8 CTAs per request shares the host-row copies)",
             "mtp": {
                 "workload": "multi-token verify step of 8 requests: 7 query rows each (1 + 6 "
                             "drafts), k=256 per row, hot buffers of 8 x 256 rows of 656 bytes, "
