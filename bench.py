@@ -60,6 +60,9 @@ def _bf16_peak():
         return 1900.0, "fallback"
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (reported beside the measured-peak fraction)
+
+
 def _logits_traffic():
     """DRAM bytes per indexer_mqa_logits launch on the 1M verify shape from the
     committed ncu summary, if it was taken on the current logits kernel source."""
@@ -843,6 +846,8 @@ def run_ours(args):
             "kernel": "select_kernel (topk_select_paged)",
             "algorithmic_bytes_per_launch": alg_bytes,
             "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "nominal_peak": NOMINAL_HBM_GBS,
         },
         "cpu_baseline": cpu,
         "e2e": e2e,
