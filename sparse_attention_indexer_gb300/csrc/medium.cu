@@ -278,6 +278,18 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
   const unsigned long long period = (unsigned long long)P.rows + gridDim.x;
   unsigned long long pending = 0ull;  // thread 0: the claimed next ticket
   int nx = -1;                        // thread 0: its row, once computed
+  int nx_len = -1;                    // thread 0: that row's length (read when nx is)
+  // The next row's scores are copied into the row buffer (one bulk copy, completion on
+  // row_bar) as soon as the current row no longer reads it, while the current row's
+  // slots are translated; copy_sh tells the next row to wait for it.
+  __shared__ __align__(8) uint64_t row_bar;
+  __shared__ int copy_sh;
+  uint32_t row_phase = 0u;
+  if (threadIdx.x == 0) {
+    mbar_init(&row_bar, 1);
+    fence_mbar_init();
+    copy_sh = 0;
+  }
   // ticket -> row; a 32-bit remainder while the ticket counter fits (the 64-bit one is
   // a long software sequence on thread 0's path, which the CTA waits for)
   auto row_of = [&](unsigned long long tk) {
@@ -298,6 +310,17 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
     __syncthreads();
     const int r = row_sh;
     if (r >= P.rows) break;
+    const bool copied = copy_sh != 0;
+    if (copied) {
+      // the copy lands in the row buffer whatever this row turns out to need
+      bool ok = mbar_wait_bounded(&row_bar, row_phase, P.wait_ns);
+      if (__syncthreads_or(!ok)) {
+        if (threadIdx.x == 0) atomicOr(&h->status, TOPK_STATUS_TIMEOUT);
+        ok = mbar_wait_bounded(&row_bar, row_phase, P.wait_ns);
+        if (__syncthreads_or(!ok)) return;  // still in flight: leave the buffer alone
+      }
+      row_phase ^= 1u;
+    }
     int32_t* os = P.out_slots + (int64_t)r * P.k;
     int32_t* op = P.out_pos ? P.out_pos + (int64_t)r * P.k : nullptr;
     const int L = P.lens[r];
@@ -325,9 +348,21 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
     for (int i = threadIdx.x; i < kCoarseBins / 4; i += kMedThreads)
       reinterpret_cast<int4*>(S.hist)[i] = make_int4(0, 0, 0, 0);
     __syncthreads();
+    if (threadIdx.x == 0) copy_sh = 0;  // read by every thread above
     const float* row = P.scores + (int64_t)r * P.ld;
     int head = 0;  // scalar positions start here
-    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    if (copied) {
+      // its 16-byte vectors were copied ahead: histogram them from shared memory
+      const int nv = L >> 2;
+      for (int i = threadIdx.x; i < nv; i += kMedThreads) {
+        const float4 v = reinterpret_cast<const float4*>(sx)[i];
+        atomicAdd(&S.hist[coarse_digit(v.x)], 1);
+        atomicAdd(&S.hist[coarse_digit(v.y)], 1);
+        atomicAdd(&S.hist[coarse_digit(v.z)], 1);
+        atomicAdd(&S.hist[coarse_digit(v.w)], 1);
+      }
+      head = nv << 2;
+    } else if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
       // 16-byte vectors, four per thread in flight before any is used
       const float4* r4 = reinterpret_cast<const float4*>(row);
       const int nv = L >> 2;
@@ -412,7 +447,10 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       med_boundary(S, nb, need);
       if (lv == 0 && threadIdx.x == 0) {
         nx = row_of(pending);
-        if (nx < P.rows) med_prefetch_row(P, nx);
+        if (nx < P.rows) {
+          med_prefetch_row(P, nx);
+          nx_len = __ldg(P.lens + nx);  // first used once this row's levels are done
+        }
       }
       const uint32_t d = (uint32_t)S.bnd_digit;
       const int above = S.bnd_above, at = S.bnd_at;
@@ -549,6 +587,17 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       }
     }
     __syncthreads();
+    if (threadIdx.x == 0 && nx >= 0 && nx < P.rows && nx_len > P.k && nx_len <= P.max_len) {
+      // the row buffer is free: copy the next row's whole 16-byte vectors into it
+      const float* nrow = P.scores + (int64_t)nx * P.ld;
+      const uint32_t bytes = (uint32_t)(nx_len >> 2) * 16u;
+      if ((reinterpret_cast<uintptr_t>(nrow) & 15u) == 0 && bytes > 0) {
+        fence_proxy_async_smem();  // after this CTA's reads and writes of the buffer
+        mbar_arrive_expect_tx(&row_bar, bytes);
+        bulk_g2s(sx, nrow, bytes, &row_bar);
+        copy_sh = 1;
+      }
+    }
     med_translate(P, S, os, op, t, min(S.emitted, kr), false);
     __syncthreads();
     if (threadIdx.x == 0) {
