@@ -334,13 +334,21 @@ __global__ void __launch_bounds__(kMedThreads, 3) medium_kernel(const __grid_con
       os[i] = -1;
       if (op) op[i] = -1;
     }
-    if (kr == 0) continue;
+    // A row that ends here drops the copy flag itself (the main path does so below):
+    // every thread read it at the row's start, or it is already 0.
+    if (kr == 0) {
+      if (threadIdx.x == 0) copy_sh = 0;
+      continue;
+    }
     const int t = P.row_to_table ? P.row_to_table[r] : r;
 
     if (L <= P.k) {  // every position is taken: the scores are not read
       med_translate(P, S, os, op, t, kr, true);
       __syncthreads();
-      if (threadIdx.x == 0 && S.status) atomicOr(&h->status, S.status);
+      if (threadIdx.x == 0) {
+        if (S.status) atomicOr(&h->status, S.status);
+        copy_sh = 0;
+      }
       continue;
     }
 

@@ -148,6 +148,30 @@ def test_medium_one_plan_many_calls_and_forced_chunk():
     compare_with_oracle(b, 100, slots, pos)
 
 
+def test_medium_rows_copied_ahead_with_error_and_short_rows():
+    """Many more rows than CTAs: each CTA copies its next row into shared memory while
+    it finishes the current one. Rows too long for the table (their copy is issued,
+    then the row reports the table width and writes -1), rows no longer than k (no
+    copy, every position taken) and ordinary rows are interleaved."""
+    rng = np.random.default_rng(41)
+    rows, L = 1500, 3000
+    lens = rng.integers(50, L + 1, rows).astype(np.int32)
+    s = rng.standard_normal((rows, L)).astype(np.float32)
+    b = _batch("medium_copied", s, lens, L, seed=42, r2t=True)
+    narrow = W.Batch(b.name, b.scores, b.lens, b.max_len, b.k, b.block_table[:, :40].copy(),
+                     b.row_to_table, b.page_size)  # 2560 positions: longer rows fail
+    k = 128
+    slots, pos, st = run_gpu(narrow, k=k)
+    bad = lens > 40 * 64
+    assert bad.any() and (lens <= k).any()
+    assert st == B.STATUS_TABLE_WIDTH, B.status_str(st)
+    assert np.all(slots[bad] == -1) and np.all(pos[bad] == -1)
+    ok = np.nonzero(~bad)[0]
+    sub = W.Batch("medium_copied_ok", narrow.scores[ok].copy(), lens[ok].copy(), L, k,
+                  narrow.block_table, narrow.row_to_table[ok].copy(), 64)
+    compare_with_oracle(sub, k, slots[ok], pos[ok])
+
+
 def test_medium_status_errors_and_plan_mismatch():
     rng = np.random.default_rng(2)
     L = 5000
