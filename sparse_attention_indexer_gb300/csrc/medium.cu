@@ -19,7 +19,9 @@
 // are skipped. Once few values remain they are kept in a position list, so later
 // levels do not rescan the row. Values are emitted through warp-aggregated shared
 // counters (the order of a row's entries is unspecified) and translated to slots on
-// the way out.
+// the way out. While a row's slots are translated, the CTA's next row is already
+// being copied into the row buffer by one bulk copy (its scores were prefetched into
+// L2 earlier in the row), so the next row starts on data in shared memory.
 #include <cuda_runtime.h>
 
 #include <algorithm>
