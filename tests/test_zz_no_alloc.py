@@ -73,6 +73,24 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         compare_with_oracle(call.b, call.k, s, p)
 
 
+def test_noalloc_register_and_medium_paths():
+    """Batches that the register path (rows of at most 256 values) and the medium path
+    (at most 16384) take, back to back on the static scratch: their plans are the
+    header alone, and the medium path's row tickets carry from call to call."""
+    pr = W.pr1()
+    tiny = [t for t in W.tiny_rows() if t.rows <= B.STATIC_MAX_ROWS][:2]
+    assert len(tiny) == 2
+    calls = [_Call(pr, pr.k), _Call(tiny[0], tiny[0].k), _Call(pr, 100), _Call(tiny[1], tiny[1].k),
+             _Call(pr, 2048)]
+    for call in calls:  # back to back on one stream, no sync in between
+        assert call.run() == 0
+    torch.cuda.synchronize()
+    for i, call in enumerate(calls):
+        s, p, st = call.result()
+        assert st == 0, f"call {i}: " + B.status_str(st)
+        compare_with_oracle(call.b, call.k, s, p)
+
+
 def test_noalloc_status_reaches_the_caller_and_the_next_call_clears_it():
     """Device status bits of a call arrive in the caller's status word; the next call
     starts from a clean status. rows == 0 and status == NULL are accepted."""
