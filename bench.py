@@ -789,6 +789,9 @@ def run_ours(args):
             "verify_1m_plan_select_eager": round(float(np.mean(e_step)) * 1e3, 2),
             "verify_80k_plan_select_eager": round(float(np.mean(e_step80)) * 1e3, 2),
             "pages_topk_v2": {"80k": PAGES_80K_US, "1m": PAGES_1M_US},
+            "kernels": {"verify_80k": "rowcluster_kernel: one 8-CTA cluster per row "
+                                      "(header-only plan)",
+                        "verify_1m": "select_kernel: 21 CTAs per row, work-list plan"},
             "retimed": list(RETIMED),
         },
         "configs": dict(note="plan + select (one CUDA graph per call), L2 flushed before each "

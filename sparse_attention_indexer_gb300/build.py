@@ -1,6 +1,6 @@
 """Builds the CUDA library libtopk_paged.so in-tree for sm_103a with nvcc.
 
-Nine translation units are compiled in parallel and linked into one shared library
+Ten translation units are compiled in parallel and linked into one shared library
 that exports the C ABI of include/topk_paged.h, include/indexer_prologue.h,
 include/indexer_logits.h and include/hisparse_resolver.h (no torch types cross it).
 """
@@ -17,8 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtopk_paged.so")
-SOURCES = ["select.cu", "short.cu", "medium.cu", "plan.cu", "abi.cu", "noalloc.cu", "prologue.cu",
-           "resolver.cu", "logits.cu"]
+SOURCES = ["select.cu", "short.cu", "medium.cu", "rowcluster.cu", "plan.cu", "abi.cu", "noalloc.cu",
+           "prologue.cu", "resolver.cu", "logits.cu"]
 HEADERS = ["common.cuh", "keys.cuh", "plan_logic.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

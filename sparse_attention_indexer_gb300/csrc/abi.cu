@@ -19,6 +19,7 @@ int short_max_len();
 cudaError_t launch_short(const SelectParams& p, cudaStream_t stream);
 int medium_max_len();
 cudaError_t launch_medium(const SelectParams& p, int sms, cudaStream_t stream);
+cudaError_t launch_rowcluster(const SelectParams& p, cudaStream_t stream);
 }  // namespace topk
 
 using namespace topk;
@@ -60,6 +61,36 @@ int device_grid(int* grid) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Workspaces whose latest plan had a forced chunk (topk_plan_ex). A select on one of
+// them runs the work-list kernel where an unforced plan would take the cluster path,
+// so that a forced chunk still drives the rows through the multi-CTA path. Results
+// never depend on it: the cluster kernel needs only the plan's header, which every
+// plan writes.
+constexpr int kForcedSlots = 64;
+std::mutex g_forced_mu;
+const void* g_forced[kForcedSlots];
+int g_forced_next;
+
+void note_plan(const void* ws, bool forced) {
+  std::lock_guard<std::mutex> lk(g_forced_mu);
+  for (int i = 0; i < kForcedSlots; ++i)
+    if (g_forced[i] == ws) {
+      if (!forced) g_forced[i] = nullptr;
+      return;
+    }
+  if (forced) {
+    g_forced[g_forced_next] = ws;
+    g_forced_next = (g_forced_next + 1) % kForcedSlots;
+  }
+}
+
+bool plan_forced(const void* ws) {
+  std::lock_guard<std::mutex> lk(g_forced_mu);
+  for (int i = 0; i < kForcedSlots; ++i)
+    if (g_forced[i] == ws) return true;
+  return false;
+}
+
 int plan_common(const int32_t* lens, int rows, int max_len, int chunk, void* ws, size_t ws_bytes,
                 cudaStream_t stream) {
   if (rows < 0) return TOPK_ERR_ROWS;
@@ -72,6 +103,7 @@ int plan_common(const int32_t* lens, int rows, int max_len, int chunk, void* ws,
   if (e != TOPK_OK) return e;
   if ((int64_t)max_len > (int64_t)grid * kChunkCap) return TOPK_ERR_MAX_LEN;
   if (launch_plan(lens, rows, max_len, grid, chunk, ws, stream) != cudaSuccess) return TOPK_ERR_CUDA;
+  note_plan(ws, chunk != 0);
   return TOPK_OK;
 }
 
@@ -113,11 +145,14 @@ int select_common(const float* scores, int64_t ld, const int32_t* lens, int rows
   p.wait_ns = wait_ns;
   p.skip_cta = skip_cta;
   // Batches of short rows take the register-resident path (one warp per row), batches
-  // of medium rows the medium path (one CTA per row, several per SM); the plan's header
-  // is still checked there. `grid` is one CTA per SM.
+  // of medium rows the medium path (one CTA per row, several per SM), and a few long
+  // rows the cluster path (one thread-block cluster per row) unless the plan forced a
+  // chunk; the plan's header is still checked there. `grid` is one CTA per SM.
   if (max_len <= short_max_len()) return launch_short(p, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
   if (max_len <= medium_max_len())
     return launch_medium(p, grid, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+  if (cluster_batch(rows, max_len, grid) && !plan_forced(workspace))
+    return launch_rowcluster(p, stream) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
   if (launch_select(p, grid, stream) != cudaSuccess) return TOPK_ERR_CUDA;
   return TOPK_OK;
 }

@@ -33,6 +33,7 @@ constexpr uint32_t kMagic = 0x54504B32u;   // plan magic
 constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // bounded waits: 200 ms
 constexpr int kShortMaxLen = 256;          // batches with max_len <= this: register path
 constexpr int kMediumMaxLen = 16384;       // batches with max_len <= this: one CTA per row, several per SM
+constexpr int kClusterMaxLen = 131072;     // longer ones up to this: one cluster per row, when they fit
 
 // ---------------------------------------------------------------- workspace
 // All offsets are multiples of 256 bytes.
@@ -122,6 +123,21 @@ __host__ __device__ inline Layout make_layout(int rows) {
 }
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// CTAs of the thread-block cluster that runs one row of a batch with this max_len on
+// the cluster path (2, 4 or 8: the fewest that keep a CTA's share at most
+// kClusterMaxLen / 8 values), or 0 outside that path's lengths.
+__host__ __device__ inline int cluster_size_for(int max_len) {
+  if (max_len <= kMediumMaxLen || max_len > kClusterMaxLen) return 0;
+  return max_len <= kClusterMaxLen / 4 ? 2 : max_len <= kClusterMaxLen / 2 ? 4 : 8;
+}
+
+// Whether an unforced plan of this batch sends it down the cluster path: its rows'
+// clusters fit the grid (one CTA per SM) at once. The plan is then its header alone.
+__host__ __device__ inline bool cluster_batch(int rows, int max_len, int grid) {
+  const int cs = cluster_size_for(max_len);
+  return cs > 0 && rows >= 1 && (int64_t)rows * cs <= (int64_t)grid;
+}
 
 // Chunk of `rank` among G CTAs of a row of length L: [begin, end).
 __host__ __device__ inline void chunk_range(int L, int G, int rank, int* begin, int* end) {

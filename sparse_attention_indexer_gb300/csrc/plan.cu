@@ -781,8 +781,9 @@ extern "C" int topk_trace_plan(uint64_t* host, int n) {
 #endif
 
 // Plan of a batch of short or medium rows (max_len <= kMediumMaxLen: the register path,
-// one warp per row, or the medium path, one CTA per row; no work list): the header
-// alone, which the select kernels check, with the medium path's row tickets at 0.
+// one warp per row, or the medium path, one CTA per row), or of a few long rows (the
+// cluster path, one thread-block cluster per row); no work list: the header alone,
+// which the select kernels check, with the medium path's row tickets at 0.
 __global__ void short_plan_kernel(int rows, int max_len, int grid, char* ws) {
   if (threadIdx.x != 0) return;
   Header* h = reinterpret_cast<Header*>(ws);
@@ -805,7 +806,7 @@ __global__ void short_plan_kernel(int rows, int max_len, int grid, char* ws) {
 
 cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, int chunk_force,
                         void* ws, cudaStream_t stream) {
-  if (max_len <= kMediumMaxLen && chunk_force == 0) {
+  if ((max_len <= kMediumMaxLen || cluster_batch(rows, max_len, grid)) && chunk_force == 0) {
     short_plan_kernel<<<1, 32, 0, stream>>>(rows, max_len, grid, static_cast<char*>(ws));
     return cudaGetLastError();
   }
@@ -826,7 +827,8 @@ cudaError_t launch_plan(const int32_t* lens, int rows, int max_len, int grid, in
 int plan_host(const int32_t* lens, int rows, int max_len, int grid, int chunk_force, char* ws) {
   const Layout lay = make_layout(rows);
   Header* h = reinterpret_cast<Header*>(ws + lay.header);
-  if (max_len <= kMediumMaxLen && chunk_force == 0) {  // register or medium path: header only
+  if ((max_len <= kMediumMaxLen || cluster_batch(rows, max_len, grid)) && chunk_force == 0) {
+    // register, medium or cluster path: header only
     *h = Header{};
     h->magic = kMagic;
     h->rows = rows;

@@ -144,20 +144,21 @@ def test_expired_wait_ends_the_call_and_a_new_plan_recovers():
     with a 2 ms limit the other CTAs of that row give up, the call ends, the status
     reports TOPK_STATUS_TIMEOUT and the first expired wait is recorded (kind 1, that
     row). Rows served by other CTAs are exact. A new plan then gives an exact call on
-    the same workspace."""
+    the same workspace (here an automatic one: the cluster path)."""
     from tests.test_plan_host import parse_plan
     b = W.verify_80k()
     dev = to_dev(b)
     grid = B.topk_grid_size()
+    chunk = 4096  # the work-list kernel, 20 CTAs per row
     img = np.zeros(B.topk_workspace_bytes(b.rows, b.max_len), np.uint8)
-    B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img)
+    B.topk_plan_host(b.lens, b.rows, b.max_len, grid, chunk, img)
     _, _, _, (_, units), info = parse_plan(img, b.rows)
     # wave 0, CTA 1: a rank of a split row (row, s0, n, len, rank, G, group)
     skip = 1
     row_of_skip, g_of_skip = int(units[skip, 0]), int(units[skip, 5])
     assert row_of_skip >= 0 and g_of_skip >= 2
     core = PagedTopK(b.rows, b.max_len)
-    core.plan(dev[1])
+    core.plan(dev[1], chunk=chunk)
     slots, pos, st = run_gpu(b, plan=core, dev_inputs=dev, wait_ns=2_000_000, skip_cta=skip)
     assert st & B.STATUS_TIMEOUT, B.status_str(st)
     diag = core.workspace[128:160].cpu().numpy().view(np.int32)

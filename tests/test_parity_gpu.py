@@ -210,7 +210,7 @@ def test_slots_only_output():
 
 
 def test_device_plan_matches_host_reference():
-    from tests.test_plan_host import parse_plan
+    from tests.test_plan_host import header_only, parse_plan
     grid = B.topk_grid_size()
     mixed = W.mixed_decode()
     few = _subset(mixed, np.arange(20))   # one-warp planner, one row per lane, both row kinds
@@ -229,8 +229,10 @@ def test_device_plan_matches_host_reference():
                      [3000 + 977 * i for i in range(63)], spread(500), spread(700),
                      err_rows)]
     pf = W.prefill()
-    # the medium batches on the full planner: a max_len above the medium range
-    wide = [types.SimpleNamespace(lens=x.lens, rows=x.rows, max_len=16385) for x in (W.pr1(), pf)]
+    # the medium batches on the full planner (a max_len above the cluster range), and
+    # on the cluster path
+    wide = [types.SimpleNamespace(lens=x.lens, rows=x.rows, max_len=m) for x in (W.pr1(), pf)
+            for m in (16385, 131073)]
     for b in (W.verify_80k(), W.verify_1m(), mixed, W.adversarial(), W.pr1(), few, more,
               W.tiny_rows()[0], W.tiny_rows()[15], pf, *wide, *big):
         lens = torch.from_numpy(b.lens).cuda()
@@ -241,7 +243,7 @@ def test_device_plan_matches_host_reference():
         B.topk_plan_host(b.lens, b.rows, b.max_len, grid, 0, img_host)
         hd, rd, sd, (fd, ud), info = parse_plan(img_dev, b.rows)
         hh, rh, sh, (fh, uh), _ = parse_plan(img_host, b.rows)
-        if b.max_len <= 16384:  # register or medium path: the plan is its header alone
+        if header_only(b.rows, b.max_len, grid):  # register, medium or cluster path
             assert hd == hh
             continue
         if b.rows == len(err_rows) and b.max_len > 48_128:
@@ -287,9 +289,9 @@ def test_status_errors():
 
 def test_plan_mismatch_is_reported():
     """A full plan records every row's length; a select with other lengths reports the
-    mismatch. (Plans of the register and medium paths are the header alone: they hold
-    no lengths, and any lengths up to max_len are served exactly.)"""
-    b = dataclasses.replace(W.with_ld(W.pr1(), 16388), max_len=16385)
+    mismatch. (Plans of the register, medium and cluster paths are the header alone:
+    they hold no lengths, and any lengths up to max_len are served exactly.)"""
+    b = dataclasses.replace(W.with_ld(W.pr1(), 131076), max_len=131073)
     scores, lens, table, r2t = to_dev(b)
     core = PagedTopK(b.rows, b.max_len)
     core.plan(lens)

@@ -19,7 +19,23 @@ B = S.binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER_ONLY_MAX_LEN = 16384  # batches of rows at most this long: register or medium path
-ABOVE_MEDIUM = HEADER_ONLY_MAX_LEN + 1  # a max_len that keeps a batch on the full planner
+CLUSTER_MAX_LEN = 131072     # longer ones up to this: cluster path when their clusters fit
+ABOVE_MEDIUM = CLUSTER_MAX_LEN + 1  # a max_len that keeps a batch on the full planner
+
+
+def cluster_size(max_len):
+    """CTAs per row on the cluster path (the library's rule), 0 outside its lengths."""
+    if max_len <= HEADER_ONLY_MAX_LEN or max_len > CLUSTER_MAX_LEN:
+        return 0
+    return 2 if max_len <= CLUSTER_MAX_LEN // 4 else 4 if max_len <= CLUSTER_MAX_LEN // 2 else 8
+
+
+def header_only(rows, max_len, grid, chunk=0):
+    """Whether the plan is its header alone: the register, medium or cluster path."""
+    if chunk:
+        return False
+    cs = cluster_size(max_len)
+    return max_len <= HEADER_ONLY_MAX_LEN or (cs > 0 and rows >= 1 and rows * cs <= grid)
 
 
 def _lib_or_skip():
@@ -77,9 +93,9 @@ def check_plan(lens, max_len, grid, chunk=0):
     counts one claim per remaining single row plus one failing claim per CTA."""
     _lib_or_skip()
     hdr, ri, singles, (first, units), info = host_plan(lens, max_len, grid, chunk)
-    if max_len <= HEADER_ONLY_MAX_LEN and chunk == 0:
-        # register path (one warp per row) or medium path (one CTA per row): the plan is
-        # its header alone
+    if header_only(len(lens), max_len, grid, chunk):
+        # register path (one warp per row), medium path (one CTA per row) or cluster
+        # path (one thread-block cluster per row): the plan is its header alone
         assert hdr["magic"] == 0x54504B32 and hdr["rows"] == len(lens)
         assert hdr["max_len"] == max_len and hdr["status"] == 0 and hdr["plan_error"] == 0
         assert hdr["waves"] == 0 and hdr["n_multi"] == 0 and hdr["n_single"] == len(lens)
@@ -147,18 +163,45 @@ def check_plan(lens, max_len, grid, chunk=0):
 
 @pytest.mark.parametrize("grid", [152, 148, 132])
 def test_plan_verify_configs_fit_one_wave(grid):
-    for b in (W.verify_80k(), W.verify_1m()):
-        hdr, ri = check_plan(b.lens, b.max_len, grid)
-        need = sum(-(-int(l) // B.topk_chunk_capacity()) for l in b.lens)
-        if need <= grid:  # one wave whenever the rows can fit the grid at all
-            assert hdr["waves"] == 1
-            assert int(ri[:, 1].sum()) <= grid
+    b = W.verify_1m()
+    hdr, ri = check_plan(b.lens, b.max_len, grid)
+    need = sum(-(-int(l) // B.topk_chunk_capacity()) for l in b.lens)
+    if need <= grid:  # one wave whenever the rows can fit the grid at all
+        assert hdr["waves"] == 1
+        assert int(ri[:, 1].sum()) <= grid
+    # the 80K verify batch runs on the cluster path (7 clusters of 8): header only
+    b = W.verify_80k()
+    hdr, ri = check_plan(b.lens, b.max_len, grid)
+    assert ri is None and hdr["waves"] == 0
 
 
 def test_plan_80k_spreads_rows_over_the_grid():
+    """On the work-list planner (too many rows for the cluster path, or a grid too small
+    for its clusters), 80K rows are split over many CTAs each."""
     b = W.verify_80k()
-    hdr, ri = check_plan(b.lens, b.max_len, 152)
-    assert all(int(g) >= 16 for g in ri[:, 1])
+    lens = np.concatenate([b.lens] * 3)  # 21 rows: 168 cluster CTAs > 152
+    hdr, ri = check_plan(lens, b.max_len, 152)
+    assert ri is not None and all(int(g) >= 7 for g in ri[:, 1])
+    hdr, ri = check_plan(b.lens, b.max_len, 48)  # 56 cluster CTAs > 48
+    assert ri is not None and hdr["waves"] == 1
+
+
+def test_plan_cluster_path_rule():
+    """Header-only plans for batches whose clusters (2, 4 or 8 CTAs per row by max_len)
+    fit the grid; the full planner for a forced chunk, more rows, or longer rows."""
+    _lib_or_skip()
+    for max_len, cs in ((16385, 2), (32768, 2), (32769, 4), (65536, 4), (65537, 8), (131072, 8)):
+        assert cluster_size(max_len) == cs
+        rows = 152 // cs
+        lens = np.full(rows, max_len, np.int32)
+        hdr, ri = check_plan(lens, max_len, 152)
+        assert ri is None and hdr["n_single"] == rows
+        hdr, ri = check_plan(np.full(rows + 1, max_len, np.int32), max_len, 152)
+        assert ri is not None
+        hdr, ri = check_plan(lens, max_len, 152, chunk=8192)
+        assert ri is not None
+    hdr, ri = check_plan(np.full(3, 131073, np.int32), 131073, 152)
+    assert ri is not None
 
 
 def test_plan_all_workloads():
@@ -264,6 +307,8 @@ def test_auto_chunk_is_smallest_fitting(grid):
              rng.integers(0, 60_000, size=300).astype(np.int32)]
     for lens in cases:
         max_len = int(max(lens.max(), 1))
+        if header_only(len(lens), max_len, grid):
+            max_len = ABOVE_MEDIUM  # the same lengths on the work-list planner
         hdr, _ = check_plan(lens, max_len, grid) if grid * cap >= max_len else (None, None)
         if hdr is None:
             continue

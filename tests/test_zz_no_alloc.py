@@ -46,9 +46,10 @@ class _Call:
 
 
 def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
-    a = W.verify_80k()                       # 7 rows of 80K: multi-CTA rows
+    a = W.verify_80k()                       # 7 rows of 80K: the cluster path
     c = W.adversarial(rows=B.STATIC_MAX_ROWS, max_len=32768)  # at the row limit
-    calls = [_Call(a, a.k), _Call(c, 512), _Call(a, 100)]
+    m = W.mixed_decode()                     # 64 rows up to 200K: the work-list kernel
+    calls = [_Call(a, a.k), _Call(c, 512), _Call(m, 2048), _Call(a, 100)]
     calls[0].run()  # first call per device does the set-up; results checked below
     torch.cuda.synchronize()
     alloc0 = torch.cuda.memory_allocated()
