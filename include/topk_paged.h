@@ -91,12 +91,17 @@ int topk_chunk_capacity(void);
  * topk_workspace_bytes(rows, max_len) bytes). The batch's max_len picks the path:
  *   - max_len <= 256: one warp per row, the row in registers;
  *   - max_len <= 16384: one CTA per row, several CTAs per SM, the row in shared memory;
+ *   - max_len <= 131072 with rows * C <= topk_grid_size(), where C = 2, 4 or 8 CTAs
+ *     per row for max_len up to 32768, 65536 or 131072: one thread-block cluster of C
+ *     CTAs per row, each CTA holding a range of the row's positions in shared memory;
+ *     the CTAs merge their histograms through distributed shared memory;
  *   - otherwise every row is binned by length into a single-CTA path (the row
  *     resident in one CTA's shared memory) or a multi-CTA path (the row split into
  *     chunks processed by co-resident CTAs that combine their histograms through
  *     global memory), and the plan holds that work list.
- * For the first two paths the plan is its header alone (a forced chunk, see
- * topk_plan_ex, still builds the work list, which those paths do not read). Rows with
+ * For the first three paths the plan is its header alone. A forced chunk (see
+ * topk_plan_ex) builds the work list; the register and medium paths do not read it,
+ * and a batch of the cluster path then runs on the work list instead. Rows with
  * len <= k are copied whole on every path. Also resets the workspace counters and the
  * status word.
  *
@@ -115,9 +120,12 @@ int topk_plan(const int32_t* lens, int rows, int max_len, void* workspace,
 int topk_plan_ex(const int32_t* lens, int rows, int max_len, int chunk, void* workspace,
                  size_t ws_bytes, topk_stream_t stream);
 
-/* Select + page translation (one launch of a persistent, co-resident grid).
- *   scores      device fp32 [rows, ld], row-major, 4-byte aligned; only the first
- *               lens[r] entries of row r are read (in whole aligned 16-byte vectors)
+/* Select + page translation (one launch: the path the plan's batch falls in).
+ *   scores      device fp32 [rows, ld], row-major, 4-byte aligned; entries past
+ *               lens[r] never affect the result. The cluster path copies a row's
+ *               whole aligned 16-byte vectors below max_len before it reads lens[r]
+ *               (memory inside the row's stride, as ld >= max_len); the other paths
+ *               read the first lens[r] entries (in whole aligned 16-byte vectors)
  *   ld          row stride in elements, ld >= max_len
  *   lens        device int32 [rows]: must equal the lens given to topk_plan
  *   k           1 <= k <= TOPK_MAX_K

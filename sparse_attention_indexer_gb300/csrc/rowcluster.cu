@@ -10,9 +10,10 @@
 // [c * chunk, (c + 1) * chunk), so the CTA ranks order the positions.
 //
 // Per row:
-//  1. Each CTA bulk-copies its share (whole 16-byte vectors up to max_len, in 8 KB
-//     pieces with one mbarrier each) into shared memory as soon as it starts, before
-//     the row's length is read, and histograms the 12-bit coarse digit as pieces land.
+//  1. Each CTA loads its share (whole 16-byte vectors below max_len, eight per thread
+//     in flight) as soon as it starts, before the row's length is read; once the length
+//     is known it stores the row's values into shared memory and histograms their 12-bit
+//     coarse digit.
 //  2. Cluster barrier. Every CTA reads the peers' histograms through the cluster's
 //     shared window and finds the same boundary bin: first over the 64 super-bin
 //     totals, then over the 64 bins of the super-bin that holds it. The same reads
@@ -31,8 +32,7 @@
 //
 // Every decision that decides a barrier is taken from merged counts, so all CTAs of a
 // cluster pass the same barriers. A CTA's shared memory is read by its peers only
-// before the barrier that ends the row, and every piece copy is waited for (bounded)
-// before a CTA ends.
+// before the barrier that ends the row.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -48,8 +48,7 @@ constexpr int kClThreads = 512;
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClPer = kClusterMaxLen / 8;        // values of one CTA's share, at most
 constexpr int kClSteps = kClPer / kClThreads;     // value s * kClThreads + t is bit s of thread t
-constexpr int kClPiece = 2048;                    // floats per bulk copy (8 KB), one mbarrier each
-constexpr int kClPieces = kClPer / kClPiece;
+constexpr int kClVec = kClPer / 4 / kClThreads;  // 16-byte vectors of a share per thread
 constexpr int kClCap = 4096;                      // boundary values gathered for the ranking
 constexpr int kClRankMax = 1024;                  // up to this many: every CTA holds them all and ranks its own
 constexpr int kClFinish = 256;                    // one warp ranks lists of at most this many
@@ -57,11 +56,10 @@ constexpr int kClLevels = 5;                      // coarse digit, then the 4 ke
 constexpr int kClSegs = kClLevels + 1;            // staged output ranges: one per level, one for ties
 
 static_assert(kClSteps == 32, "a thread's values of a share fit one 32-bit mask");
-static_assert(kClPiece % kClThreads == 0, "a piece is whole steps");
+static_assert(kClVec * 4 * kClThreads == kClPer, "a share is whole vectors per thread");
 static_assert(kClPer <= 65536, "local indices fit uint16");
 
 struct __align__(16) ClShared {
-  uint64_t bar[kClPieces];      // one per piece copy (phase 0 only)
   int hist[kBins0];             // coarse histogram; its first 256 bins serve the even key levels
   int hist_odd[256];            // odd key levels; CTA 0's candidate ranking
   int sup[64];                  // coarse super-bin totals (64 bins each), read by the peers
@@ -78,7 +76,7 @@ struct __align__(16) ClShared {
   int warp_tot[kClWarps];
   int n_tpos, n_tlist;
   int bnd_d, bnd_above, bnd_at, bnd_ok;
-  int len, trow, hdr_ok, status, tmo, npieces, ncopied;
+  int len, trow, hdr_ok, status;
 };
 static_assert(sizeof(ClShared) % 16 == 0, "the share buffer after it is 16-byte aligned");
 
@@ -415,22 +413,20 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
   const float* row = P.scores + (int64_t)r * P.ld;
   CL_MARK(0);
 
+  // The share's whole vectors below max_len (inside the row's stride), eight per thread
+  // in flight, before anything else; an unaligned row is read later with plain loads.
+  int nv = min(c0 + A.chunk, P.max_len) - c0;
+  nv = nv > 0 ? nv >> 2 : 0;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0) nv = 0;
+  const float4* const row4 = reinterpret_cast<const float4*>(row + c0);
+  float4 v[kClVec];
+#pragma unroll
+  for (int j = 0; j < kClVec; ++j) {
+    const int vi = tid + j * kClThreads;
+    if (vi < nv) v[j] = __ldg(row4 + vi);
+  }
   if (tid == 0) {
-    // The share's copies first (whole vectors below max_len: inside the row's stride),
-    // then the row's length, its table row and the plan header, one round trip.
-    for (int q = 0; q < kClPieces; ++q) mbar_init(&S.bar[q], 1);
-    fence_mbar_init();
-    int nf = min(c0 + A.chunk, P.max_len) - c0;
-    nf = nf > 0 ? nf & ~3 : 0;
-    if ((reinterpret_cast<uintptr_t>(row) & 15u) != 0) nf = 0;
-    const int np = (nf + kClPiece - 1) / kClPiece;
-    for (int q = 0; q < np; ++q) {
-      const uint32_t bytes = (uint32_t)min(kClPiece, nf - q * kClPiece) * 4u;
-      mbar_arrive_expect_tx(&S.bar[q], bytes);
-      bulk_g2s(sx + q * kClPiece, row + c0 + q * kClPiece, bytes, &S.bar[q]);
-    }
-    S.npieces = np;
-    S.ncopied = nf;
+    // the row's length, its table row and the plan header: one round trip
     const int4 h0 = __ldcg(reinterpret_cast<const int4*>(h));
     const int plan_error = __ldcg(&h->plan_error);
     const int L = P.lens[r];
@@ -439,7 +435,6 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
     S.len = L;
     S.trow = t;
     S.status = 0;
-    S.tmo = 0;
     S.seg_start[0] = 0;
   }
   for (int i = tid; i < kBins0 / 4; i += kClThreads)
@@ -456,7 +451,6 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
   int32_t* const os = P.out_slots + (int64_t)r * P.k;
   int32_t* const op = P.out_pos ? P.out_pos + (int64_t)r * P.k : nullptr;
   const int32_t* const trow = P.table + (int64_t)S.trow * P.table_ld;
-  const int npieces = S.npieces;
 
   if (kr == 0 || L <= P.k) {
     // -1 padding, and every position when the row has no more than k: the scores are
@@ -473,18 +467,24 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
       if (op) op[o] = pv;
     }
     if (st) atomicOr(&h->status, st);
-    if (tid == 0) {
-      bool ok = true;
-      for (int q = 0; q < npieces; ++q) ok = mbar_wait_bounded(&S.bar[q], 0u, P.wait_ns) && ok;
-      if (!ok) atomicOr(&h->status, TOPK_STATUS_TIMEOUT);
-    }
     return;
   }
 
-  // ---- 1. the share: plain loads where no copy brings it, then the coarse histogram
+  // ---- 1. the share into shared memory, and its coarse histogram
   const int n_c = max(0, min(c0 + A.chunk, L) - c0);  // values of this CTA (positions c0 + i)
-  const int nf = S.ncopied;
-  for (int s0 = 0; s0 < kClSteps; s0 += 8) {
+  const int nf = 4 * nv;                              // values the vector loads brought
+#pragma unroll
+  for (int j = 0; j < kClVec; ++j) {
+    const int vi = tid + j * kClThreads;
+    if (vi < nv && 4 * vi < n_c) {
+      reinterpret_cast<float4*>(sx)[vi] = v[j];
+      const float e[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (4 * vi + c < n_c) atomicAdd(&S.hist[coarse_digit(e[c])], 1);
+    }
+  }
+  for (int s0 = 0; s0 < kClSteps; s0 += 8) {  // the rest (a short tail, or an unaligned row)
     float x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -500,17 +500,6 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
       }
     }
   }
-  constexpr int kStepsPerPiece = kClPiece / kClThreads;
-  bool landed = true;
-  for (int q = 0; q < npieces; ++q) {
-    landed = mbar_wait_bounded(&S.bar[q], 0u, P.wait_ns) && landed;
-#pragma unroll
-    for (int j = 0; j < kStepsPerPiece; ++j) {
-      const int i = (q * kStepsPerPiece + j) * kClThreads + tid;
-      if (i < n_c && i < nf) atomicAdd(&S.hist[coarse_digit(sx[i])], 1);
-    }
-  }
-  if (!landed) S.tmo = 1;
   __syncthreads();
   CL_MARK(2);
   {
@@ -667,6 +656,7 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
         keep |= (uint32_t)(!ends && dg == d) << s;
       }
     }
+    if (lv == 0) CL_MARK(11);
     before = 0;
     at_before = 0;  // lower-ranked peers' counts
     for (int p = 0; p < crank; ++p) {
@@ -677,11 +667,13 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
     const bool push = !ends && at <= kClCap;
     int tot_t, tot_k;
     const int2 off = cl_offsets(S, __popc(take), push ? __popc(keep) : 0, &tot_t, &tot_k);
+    if (lv == 0) CL_MARK(12);
     if (tid == 0) {
       S.seg_start[nseg] = n_elist;
       S.seg_base[nseg] = emitted + before;
     }
     cl_stage(S, take, n_elist + off.x);
+    if (lv == 0) CL_MARK(13);
     n_elist += tot_t;
     ++nseg;
     if (ends) {
@@ -816,11 +808,7 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
   if (st) atomicOr(&S.status, st);
   __syncthreads();
   if (tid == 0) {
-    int s = S.status;
-    if (S.tmo) {
-      s |= TOPK_STATUS_TIMEOUT;
-      for (int q = 0; q < npieces; ++q) (void)mbar_wait_bounded(&S.bar[q], 0u, P.wait_ns);
-    }
+    const int s = S.status;
     if (s) atomicOr(&h->status, s);
   }
 #ifdef TOPK_TRACE
