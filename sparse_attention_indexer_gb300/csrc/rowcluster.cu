@@ -631,13 +631,21 @@ __global__ void __launch_bounds__(kClThreads, 1) rowcluster_kernel(const __grid_
         // top bin has nothing above it
         const float t_at = skip_below((uint32_t)d);
         const float t_above = d < 4095 ? skip_below((uint32_t)d + 1u) : __int_as_float(0x7FC00000);
-        for (int s = 0; s * kClThreads < n_c; ++s) {
-          const int i = s * kClThreads + tid;
-          if (i >= n_c) break;
-          const float x = sx[i];
-          const bool a = x >= t_above, g = x >= t_at;
-          take |= (uint32_t)(a || (ends && g)) << s;
-          keep |= (uint32_t)(!ends && g && !a) << s;
+        const int nsteps = (n_c + kClThreads - 1) / kClThreads;  // <= kClSteps
+        for (int s0 = 0; s0 < nsteps; s0 += 4) {  // four steps' reads in flight; s0 + 3 < 32
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = (s0 + u) * kClThreads + tid;
+            x[u] = __int_as_float(0x7FC00000);  // past the share: NaN is neither taken nor kept
+            if (i < n_c) x[u] = sx[i];
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool a = x[u] >= t_above, g = x[u] >= t_at;
+            take |= (uint32_t)(a || (ends && g)) << (s0 + u);
+            keep |= (uint32_t)(!ends && g && !a) << (s0 + u);
+          }
         }
       } else {
         for (int s = 0; s * kClThreads < n_c; ++s) {
