@@ -20,15 +20,18 @@
 //     give each peer's count above the boundary and at it.
 //  3. Each CTA stages its values above the boundary; their output range starts after
 //     the lower-ranked peers' counts. Unless the boundary bin completes the row, its
-//     values are written into CTA 0's candidate list at offsets from the lower-ranked
-//     peers' counts at the boundary.
+//     values are written as (key, position) into every CTA's candidate list, at
+//     offsets from the lower-ranked peers' counts at the boundary (into CTA 0's list
+//     alone when there are more than kClRankMax of them).
 //  4. A second cluster barrier. Each CTA translates its staged positions to slots and
-//     writes them; CTA 0 ranks the candidates by (key, position) and writes the ones
-//     the row still needs.
-// A boundary bin with more values than CTA 0's list holds is refined by the whole
-// cluster, one key byte per level (a cluster barrier and a merged 256-bin histogram
-// each), before step 3. Values whose keys are still all equal after the last byte are
-// taken in position order: CTA by CTA, each CTA's first ones.
+//     writes them, and ranks its own candidates against the whole list by counting:
+//     a rank below what the row still needs is the candidate's output index. (A longer
+//     list is ranked by CTA 0 alone: radix levels over the composite key's bytes, then
+//     one warp.)
+// A boundary bin with more values than the candidate list holds (kClCap) is refined by
+// the whole cluster, one key byte per level (a cluster barrier and a merged 256-bin
+// histogram each), before step 3. Values whose keys are still all equal after the last
+// byte are taken in position order: CTA by CTA, each CTA's first ones.
 //
 // Every decision that decides a barrier is taken from merged counts, so all CTAs of a
 // cluster pass the same barriers. A CTA's shared memory is read by its peers only
@@ -233,7 +236,7 @@ __device__ __forceinline__ void cl_push(ClShared& S, const float* sx, uint32_t m
   }
 }
 
-// Slot of position p through table row trow; sets status bits of bad entries.
+// Slot of position p, whose page's table entry is pg; sets status bits of bad entries.
 __device__ __forceinline__ int32_t cl_slot(const SelectParams& P, int32_t pg, int p, int* st) {
   const int ps = P.page_size;
   const int in = (ps & (ps - 1)) == 0 ? (p & (ps - 1)) : p % ps;
