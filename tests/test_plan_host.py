@@ -202,6 +202,16 @@ def test_plan_cluster_path_rule():
         assert ri is not None
     hdr, ri = check_plan(np.full(3, 131073, np.int32), 131073, 152)
     assert ri is not None
+    # the limit follows the grid: C * rows CTAs at most, one per SM
+    for grid in (148, 132, 37):
+        for max_len, cs in ((20000, 2), (50000, 4), (100000, 8)):
+            rows = grid // cs
+            if rows == 0:
+                continue
+            hdr, ri = check_plan(np.full(rows, max_len, np.int32), max_len, grid)
+            assert ri is None, (grid, max_len)
+            hdr, ri = check_plan(np.full(rows + 1, max_len, np.int32), max_len, grid)
+            assert ri is not None, (grid, max_len)
 
 
 def test_plan_all_workloads():
